@@ -1,0 +1,222 @@
+/*
+ * specverify.h -- C ABI of libspecverify: batched speculative-decoding
+ * verification on one GB300 (sm_103a).
+ *
+ * Source of the method: "Accelerating Sonar through speculation"
+ * (Perplexity blog), sections "Speculative decoding", "Target-Draft",
+ * "EAGLE", "MTP" and "MTP schedule for a single token", and the rule of the
+ * work it cites first, "Fast Inference from Transformers via Speculative
+ * Decoding": accept a drafted token x with probability min(1, p(x)/q(x));
+ * at the first rejection draw from norm(max(0, p - q)); after a full accept
+ * draw a bonus token from the target's last row.
+ *
+ * Conventions shared by every call:
+ *  - Every array argument is a DEVICE pointer owned by the caller, except
+ *    `params`, which is a host pointer read before the call returns.  The
+ *    library allocates nothing and keeps no state between calls.
+ *  - Work is enqueued on `stream` (NULL = the legacy default stream) and
+ *    the call returns without synchronising.  Outputs are valid once the
+ *    stream reaches that point.
+ *  - Host-detectable errors (NULL required pointer, bad size, unsupported
+ *    combination, workspace too small) are returned synchronously and
+ *    nothing is enqueued.  SPEC_ERR_CUDA reports a failed launch.
+ *  - Data-dependent errors found on the device (token id outside [0, V),
+ *    NaN or +inf logits, a row with no finite entry, a malformed parent
+ *    array, an out-of-range accepted length) OR a SPEC_DEVERR_* bit into
+ *    *dev_error (zeroed by the call first) and give that request a defined
+ *    fallback result (see each call).  The library never traps.
+ *  - Logit rows are contiguous: element (b, i, v) sits at
+ *    ((b * rows + i) * V + v).  V need not be a multiple of 8.
+ *  - Random draws use counter-based Philox4x32-10 (Salmon, Moraes, Dror,
+ *    Shaw, SC'11): key = (seed lo32, seed hi32), counter = (request lo32,
+ *    position lo32, purpose | round << 8, request hi32), u = (word0 >> 8) *
+ *    2^-24.  Results depend only on (inputs, seed, request id, position),
+ *    never on the batch size or on a request's slot in the batch.
+ *  - Calls that overlap on the GPU must not share output or workspace
+ *    buffers.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t. */
+typedef struct CUstream_st* spec_stream_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,  /* NULL required pointer, negative size, bad params */
+    SPEC_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. size limits) */
+    SPEC_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than spec_workspace_size() */
+    SPEC_ERR_CUDA = 4          /* a CUDA call or kernel launch failed */
+} spec_status;
+
+typedef enum { SPEC_BF16 = 0, SPEC_F32 = 1 } spec_dtype;
+
+/* How the children of a draft-tree node were drawn from the draft model
+ * (section "EAGLE": Top-K candidates per node).  The residual update after
+ * a rejected child depends on it. */
+typedef enum {
+    SPEC_CHILD_WOR = 0,           /* sampled without replacement */
+    SPEC_CHILD_IID = 1,           /* sampled with replacement */
+    SPEC_CHILD_DETERMINISTIC = 2  /* the K most likely draft tokens; draft logits unused */
+} spec_child_mode;
+
+typedef enum { SPEC_OP_LINEAR = 0, SPEC_OP_TREE = 1 } spec_op;
+
+/* Philox purposes (counter word 2, low byte). */
+#define SPEC_PURPOSE_ACCEPT 1
+#define SPEC_PURPOSE_RESIDUAL 2
+#define SPEC_PURPOSE_BONUS 3
+#define SPEC_PURPOSE_DRAFT 4
+
+/* Bits OR-ed into *dev_error. */
+#define SPEC_DEVERR_TOKEN 1      /* a draft/node token outside [0, V) */
+#define SPEC_DEVERR_NONFINITE 2  /* NaN or +inf logit, or no finite logit in a row */
+#define SPEC_DEVERR_PARENT 4     /* parent[] not a tree rooted at 0 with parent[i] < i, or deeper than max_depth */
+#define SPEC_DEVERR_LENGTH 8     /* compaction: accepted length or source row out of range */
+
+typedef struct {
+    float temperature;  /* 0 => greedy (argmax, ties to the lowest index); > 0 => sampled */
+    float top_p;        /* in (0, 1): nucleus filter on p and q; >= 1 => off */
+    uint64_t seed;      /* Philox key */
+    int32_t child_mode; /* spec_child_mode; tree only */
+} spec_sampling_params;
+
+/*
+ * Bytes of device workspace a call needs (16-byte alignment suffices).
+ * op = SPEC_OP_LINEAR: k_or_N = k.  op = SPEC_OP_TREE: k_or_N = N.
+ * Returns 0 for invalid sizes.
+ */
+size_t spec_workspace_size(spec_op op, int B, int k_or_N, int V, spec_dtype dtype);
+
+/*
+ * Linear verification (sections "Speculative decoding" and "Target-Draft":
+ * the target scores every prefix of the k drafted tokens; the longest
+ * accepted prefix is kept and the target's logits after it give one more
+ * token, so k drafts yield at most k+1 tokens).
+ *
+ *  target_logits [B, k+1, V]  row i scores the token after the prefix plus
+ *                             d_1..d_i (row k: after all k drafts).
+ *  draft_logits  [B, k, V]    row i is the distribution d_{i+1} was drawn
+ *                             from.  Unused (may be NULL) when
+ *                             temperature == 0.
+ *  draft_tokens  [B, k] int32 d_1..d_k.
+ *  request_ids   [B] int64 or NULL (=> b); positions [B] int64 or NULL
+ *                (=> 0): drafted token i (1-based) is at position
+ *                positions[b] + i; the emitted token t* at
+ *                positions[b] + a + 1.
+ *  params        temperature T, top_p, seed (child_mode ignored).
+ *  p = filter(softmax(target / T)), q = filter(softmax(draft / T)), filter
+ *  = the top-p nucleus in (logit desc, index asc) order (a token is kept
+ *  when the mass before it is < top_p), renormalised.
+ *  Sampled (T > 0): d_i is accepted iff u_i < p_{i-1}(d_i) / q_{i-1}(d_i)
+ *  (q == 0 rejects), u_i from purpose ACCEPT; a = number of leading
+ *  accepts.  If a < k, t* is the smallest v with C(v) > u * C(V-1), C the
+ *  running sum of max(0, p_a - q_a) in index order and u from purpose
+ *  RESIDUAL (if that residual is all zero, of p_a instead); if a == k, the
+ *  same over p_k with purpose BONUS.
+ *  Greedy (T == 0): d_i is accepted iff it is the lowest-index argmax of
+ *  target row i-1; t* = argmax of target row a.
+ *
+ *  Outputs: accepted_len [B] (a), out_tokens [B, k+1] (d_1..d_a, t*, then
+ *  -1), accept_prob [B, k] = min(1, p/q) for every drafted token (greedy:
+ *  1 or 0) or NULL, token_probs [B, k, 2] = (p_{i}(d_{i+1}),
+ *  q_{i}(d_{i+1})) or NULL, len_hist [k+1] histogram of a over the batch
+ *  (zeroed by the call) or NULL, dev_error [1] or NULL.
+ *  Invalid request (bad token, non-finite row): a = 0, t* = lowest-index
+ *  argmax of target row 0 over entries that are neither NaN nor +inf,
+ *  accept_prob and token_probs 0.
+ *  workspace: spec_workspace_size(SPEC_OP_LINEAR, B, k, V, dtype) bytes.
+ *  Limits: 1 <= B, 1 <= k <= 64, 1 <= V < 2^31 / (2k+1) / B rows*V.
+ */
+spec_status spec_verify_linear(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, int B, int k, int V,
+                               const int64_t* request_ids, const int64_t* positions,
+                               const spec_sampling_params* params,
+                               int32_t* accepted_len, int32_t* out_tokens, float* accept_prob,
+                               float* token_probs, int32_t* len_hist, int32_t* dev_error,
+                               void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * Tree verification (section "EAGLE": a static draft tree explored with the
+ * Top-K candidates of every node; the longest accepted root-to-leaf path is
+ * kept plus one target token).
+ *
+ *  target_logits [B, N, V]   row n scores the token after node n's path
+ *                            (node 0 = the root, the last committed token).
+ *  draft_logits  [B, N, V]   row n is the draft distribution the children of
+ *                            n were drawn from; may be NULL when T == 0 or
+ *                            child_mode == SPEC_CHILD_DETERMINISTIC.
+ *  node_tokens   [B, N] int32 token of each node (node 0's is ignored).
+ *  parent        [N] int32   parent[0] = -1, 0 <= parent[i] < i.  The
+ *                            children of n are tested in increasing index
+ *                            order.
+ *  max_depth     depth of the deepest node (host value; checked on the
+ *                device); outputs have W = max_depth + 1 columns.
+ *  At node n of depth t, with P = p_n and Q = q_n: child j (0-based) with
+ *  token x is accepted iff u < P(x) / Q(x) (DETERMINISTIC: u < P(x)), u from
+ *  purpose ACCEPT, round j, position positions[b] + t + 1.  After a reject:
+ *  P <- norm(max(0, P - Q)) (DETERMINISTIC: P with x removed, renormalised;
+ *  a zero residual leaves P unchanged), and Q <- Q with x removed,
+ *  renormalised (WOR) or unchanged (IID).  An accept moves to that child.
+ *  A leaf draws the bonus token from p_leaf (purpose BONUS); a node whose
+ *  children are all rejected draws t* from the final P (purpose RESIDUAL),
+ *  both by the inverse CDF above.  Greedy: descend into the first child
+ *  whose token is the lowest-index argmax of p_n, else emit that argmax.
+ *
+ *  Outputs: accepted_len [B] (accepted depth a), path_nodes [B, W] (0, the
+ *  accepted nodes, then -1), out_tokens [B, W] (their tokens, t*, then -1),
+ *  dev_error [1] or NULL.  Invalid request: a = 0, path = [0], t* = argmax
+ *  of target row 0 as for the linear call.
+ *  workspace: spec_workspace_size(SPEC_OP_TREE, B, N, V, dtype) bytes.
+ *  Limits: 1 <= N <= 1024, max_depth < N, at most 64 children per node.
+ */
+spec_status spec_verify_tree(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                             const int32_t* node_tokens, const int32_t* parent, int B, int N, int V,
+                             int max_depth, const int64_t* request_ids, const int64_t* positions,
+                             const spec_sampling_params* params, int32_t* accepted_len, int32_t* path_nodes,
+                             int32_t* out_tokens, int32_t* dev_error, void* workspace, size_t workspace_bytes,
+                             spec_stream_t stream);
+
+/*
+ * Compaction for the next draft step (section "MTP": token t_{i+1} is drawn
+ * from logits computed from hidden state H_i, so token buffers sit one step
+ * left of the hidden states; section "MTP schedule for a single token": a
+ * kernel inserts the next target tokens into their slots with no host
+ * synchronisation).
+ *
+ *  hidden       [B, T, H] 2-byte elements (bf16), copied bit for bit.
+ *  accepted_len [B]; out_tokens [B, W]; path_nodes [B, W] or NULL (NULL =>
+ *               rows 0..a_b, the linear layout).
+ *  offsets      [B+1] out: offsets[0] = 0, offsets[b+1] = offsets[b] +
+ *               a_b + 1.
+ *  out_hidden   [B*W, H] out: row offsets[b] + r = hidden[b, src_r, :],
+ *               src_r = path_nodes[b, r] (or r), r = 0..a_b.
+ *  next_tokens  [B*W] out: next_tokens[offsets[b] + r] = out_tokens[b, r]
+ *               (the token that follows the hidden row it is paired with).
+ *  A request with a_b outside [0, W-1], or a source row outside [0, T),
+ *  contributes no rows and sets SPEC_DEVERR_LENGTH.  Rows past
+ *  offsets[B] are left untouched.
+ *  Limits: H * 2 bytes must be a multiple of 16 when the hidden and output
+ *  pointers are 16-byte aligned for the vector path; other cases use a
+ *  2-byte path.  B * W < 2^31.
+ */
+spec_status spec_compact_accepted(const void* hidden, int B, int T, int H, const int32_t* accepted_len,
+                                  const int32_t* path_nodes, const int32_t* out_tokens, int W, void* out_hidden,
+                                  int32_t* offsets, int32_t* next_tokens, int32_t* dev_error,
+                                  spec_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char* spec_status_string(spec_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

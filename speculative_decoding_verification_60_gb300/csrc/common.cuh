@@ -1,0 +1,305 @@
+// Device building blocks of libspecverify (sm_103a).
+//
+// Method: "Accelerating Sonar through speculation", sections "Speculative
+// decoding", "Target-Draft", "EAGLE", "MTP"; rule of the cited "Fast
+// Inference from Transformers via Speculative Decoding".
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sv {
+
+constexpr int kNT = 1024;            // threads of every row-level CTA
+constexpr int kNW = kNT / 32;        // warps of such a CTA
+constexpr int kPurposeAccept = 1;
+constexpr int kPurposeResidual = 2;
+constexpr int kPurposeBonus = 3;
+constexpr int kPurposeDraft = 4;
+
+constexpr int kDevErrToken = 1;
+constexpr int kDevErrNonfinite = 2;
+constexpr int kDevErrParent = 4;
+constexpr int kDevErrLength = 8;
+
+// ---------------------------------------------------------------- Philox --
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
+// easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies with a
+// Weyl key schedule.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+        c = make_uint4(hi1 ^ c.y ^ k.x, lo1, hi0 ^ c.w ^ k.y, lo0);
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// u in [0, 1) on the 2^-24 grid (exact in fp32):
+// key = (seed lo, seed hi), counter = (req lo, pos lo, purpose | round << 8, req hi).
+__device__ __forceinline__ float uniform01(uint64_t seed, int64_t req, int64_t pos, int purpose, int round) {
+    const uint64_t r = (uint64_t)req;
+    const uint4 c = make_uint4((uint32_t)r, (uint32_t)(uint64_t)pos, (uint32_t)purpose | ((uint32_t)round << 8),
+                               (uint32_t)(r >> 32));
+    const uint4 o = philox4x32_10(c, make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+    return (float)(o.x >> 8) * (1.0f / 16777216.0f);
+}
+
+// ------------------------------------------------------------- numerics --
+// 2^x on the MUFU unit (flushes results below 2^-126 to zero).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Weight of logit x in a row with max m at c = log2(e) / T: 2^(x*c - m*c).
+// Every kernel forms m*c the same way so that weights agree bit for bit.
+__device__ __forceinline__ float scaled_max(float m, float c) { return m * c; }
+__device__ __forceinline__ float weight_of(float x, float c, float mc) { return ex2(fmaf(x, c, -mc)); }
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Order-preserving 16-bit key of a bf16 bit pattern (larger key = larger
+// value; NaNs sit outside [-inf, +inf]).  -0 maps one below +0.
+__device__ __forceinline__ uint32_t okey16(uint32_t b) {
+    return (b & 0x8000u) ? (~b & 0xffffu) : (b | 0x8000u);
+}
+__device__ __forceinline__ uint32_t okey16_to_bits(uint32_t k) {
+    return (k & 0x8000u) ? (k & 0x7fffu) : (~k & 0xffffu);
+}
+__device__ __forceinline__ uint32_t okey32(float f) {
+    const uint32_t b = __float_as_uint(f == 0.0f ? 0.0f : f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float okey32_to_float(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Round a float down to a bf16 value (towards -inf), as its bit pattern.
+__device__ __forceinline__ uint32_t bf16_bits_round_down(float f) {
+    uint32_t b = __float_as_uint(f);
+    const uint32_t t = b >> 16;
+    if ((b & 0xffffu) == 0u) return t;
+    return (b & 0x80000000u) ? t + 1u : t;  // negative: more negative is larger magnitude
+}
+
+// ------------------------------------------------------- block reductions --
+struct BlockScratch {
+    double d[kNW];
+    float f[kNW];
+    int i[kNW];
+    unsigned u[kNW];
+    double bcast_d[4];
+    float bcast_f[8];
+    int bcast_i[8];
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_min_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// All threads of the CTA must call these (they contain __syncthreads).
+__device__ __forceinline__ float block_max(float v, BlockScratch& s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_max(v);
+    if (lane == 0) s.f[w] = v;
+    __syncthreads();
+    float r = s.f[0];
+#pragma unroll 4
+    for (int i = 1; i < kNW; ++i) r = fmaxf(r, s.f[i]);
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ int block_min_i(int v, BlockScratch& s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_min_i(v);
+    if (lane == 0) s.i[w] = v;
+    __syncthreads();
+    int r = s.i[0];
+#pragma unroll 4
+    for (int i = 1; i < kNW; ++i) r = min(r, s.i[i]);
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ int block_sum_i(int v, BlockScratch& s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_sum_i(v);
+    if (lane == 0) s.i[w] = v;
+    __syncthreads();
+    int r = 0;
+#pragma unroll 4
+    for (int i = 0; i < kNW; ++i) r += s.i[i];
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ bool block_any(bool v, BlockScratch& s) {
+    return __syncthreads_or(v ? 1 : 0) != 0;
+}
+// Deterministic fp64 sum: fixed shuffle tree, then warp totals in order.
+__device__ __forceinline__ double block_sum_d(double v, BlockScratch& s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_sum_d(v);
+    if (lane == 0) s.d[w] = v;
+    __syncthreads();
+    double r = 0.0;
+#pragma unroll 4
+    for (int i = 0; i < kNW; ++i) r += s.d[i];
+    __syncthreads();
+    return r;
+}
+// Exclusive prefix in thread order (fp64); *total receives the sum.
+__device__ __forceinline__ double block_exclusive_scan_d(double v, BlockScratch& s, double* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    double x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s.d[w] = x;
+    __syncthreads();
+    double base = 0.0, tot = 0.0;
+    for (int i = 0; i < kNW; ++i) {
+        if (i < w) base += s.d[i];
+        tot += s.d[i];
+    }
+    __syncthreads();
+    if (total) *total = tot;
+    return base + x - v;
+}
+__device__ __forceinline__ int block_exclusive_scan_i(int v, BlockScratch& s, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) s.i[w] = x;
+    __syncthreads();
+    int base = 0, tot = 0;
+    for (int i = 0; i < kNW; ++i) {
+        if (i < w) base += s.i[i];
+        tot += s.i[i];
+    }
+    __syncthreads();
+    if (total) *total = tot;
+    return base + x - v;
+}
+
+// ------------------------------------------------------------ row access --
+// Element type traits: VEC elements per 16-byte vector.
+template <typename T> struct ElemT;
+template <> struct ElemT<__nv_bfloat16> {
+    static constexpr int VEC = 8;
+    __device__ static __forceinline__ float load(const __nv_bfloat16* p) {
+        return bf16_bits_to_float(*reinterpret_cast<const unsigned short*>(p));
+    }
+    __device__ static __forceinline__ void unpack(const uint4& v, float* o) {
+        o[0] = bf16_lo(v.x); o[1] = bf16_hi(v.x); o[2] = bf16_lo(v.y); o[3] = bf16_hi(v.y);
+        o[4] = bf16_lo(v.z); o[5] = bf16_hi(v.z); o[6] = bf16_lo(v.w); o[7] = bf16_hi(v.w);
+    }
+};
+template <> struct ElemT<float> {
+    static constexpr int VEC = 4;
+    __device__ static __forceinline__ float load(const float* p) { return *p; }
+    __device__ static __forceinline__ void unpack(const uint4& v, float* o) {
+        o[0] = __uint_as_float(v.x); o[1] = __uint_as_float(v.y);
+        o[2] = __uint_as_float(v.z); o[3] = __uint_as_float(v.w);
+    }
+};
+
+// A row split into a scalar head (until the first 16-byte boundary), a body
+// of 16-byte vectors and a scalar tail.  "Units" walk it in index order:
+// unit 0 is the head (possibly empty), units 1..nvec the vectors, unit
+// nvec+1 the tail (possibly empty).
+template <typename T>
+struct RowView {
+    const T* row;
+    int V, head, nvec, tail;
+    __device__ __forceinline__ RowView(const T* r, int v) : row(r), V(v) {
+        constexpr int VEC = ElemT<T>::VEC;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(r);
+        int h = (int)(((16u - (unsigned)(a & 15u)) & 15u) / sizeof(T));
+        if (h > V) h = V;
+        head = h;
+        nvec = (V - h) / VEC;
+        tail = V - h - nvec * VEC;
+    }
+    __device__ __forceinline__ int units() const { return nvec + 2; }
+    // Index range of unit u without loading it.
+    __device__ __forceinline__ void unit_range(int u, int& idx0, int& cnt) const {
+        constexpr int VEC = ElemT<T>::VEC;
+        if (u >= 1 && u <= nvec) { idx0 = head + (u - 1) * VEC; cnt = VEC; return; }
+        idx0 = (u == 0) ? 0 : head + nvec * VEC;
+        cnt = (u == 0) ? head : tail;
+    }
+    __device__ __forceinline__ const uint4* vec() const {
+        return reinterpret_cast<const uint4*>(row + head);
+    }
+    // Loads unit u into vals (missing slots get -inf); first element index
+    // and number of valid slots are returned through idx0 and cnt.
+    __device__ __forceinline__ void load_unit(int u, float* vals, int& idx0, int& cnt) const {
+        constexpr int VEC = ElemT<T>::VEC;
+        if (u >= 1 && u <= nvec) {
+            const uint4 v = __ldg(vec() + (u - 1));
+            ElemT<T>::unpack(v, vals);
+            idx0 = head + (u - 1) * VEC;
+            cnt = VEC;
+            return;
+        }
+        const int start = (u == 0) ? 0 : head + nvec * VEC;
+        const int n = (u == 0) ? head : tail;
+        idx0 = start;
+        cnt = n;
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) vals[j] = (j < n) ? ElemT<T>::load(row + start + j) : -INFINITY;
+    }
+};
+
+// Per-row statistics shared between kernels (32 bytes).
+struct RowStat {
+    float m;       // max logit of the row
+    float inv_zn;  // 1 / sum of weights kept (nucleus mass when top-p is on)
+    float x_tok;   // logit at the row's token of interest (NaN if none)
+    int argmax;    // lowest index holding m
+    float tau;     // top-p boundary logit; -inf when top-p is off
+    int n_keep;    // boundary-valued tokens kept (the lowest-index ones)
+    int c_tau;     // boundary-valued tokens in the row
+    int flags;     // kRowInvalid | kRowTokMember
+};
+constexpr int kRowInvalid = 1;
+constexpr int kRowTokMember = 2;
+
+// Filtered probability of a logit x given the row's statistics; `rank_ok`
+// tells whether a boundary-valued token is among the kept ones.
+__device__ __forceinline__ float filtered_prob(float x, const RowStat& st, float c, bool rank_ok) {
+    const bool member = (x > st.tau) || (x == st.tau && rank_ok);
+    return member ? weight_of(x, c, scaled_max(st.m, c)) * st.inv_zn : 0.0f;
+}
+
+}  // namespace sv

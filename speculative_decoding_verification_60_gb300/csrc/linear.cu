@@ -1,0 +1,236 @@
+// Linear verification ("Accelerating Sonar through speculation",
+// §Speculative decoding and §Target-Draft): row statistics of every target
+// and draft row, then per request the accept tests, the accepted length
+// and the residual or bonus draw.
+#include "../../include/specverify.h"
+#include "launch.cuh"
+#include "sample.cuh"
+
+namespace sv {
+
+struct LinearArgs {
+    const void* tgt;
+    const void* drf;
+    const int32_t* drafts;
+    int B, k, V;
+    const int64_t* req;
+    const int64_t* pos;
+    float T, top_p, c;
+    uint64_t seed;
+    int32_t* acc_len;
+    int32_t* out_tokens;
+    float* accept_prob;
+    float* token_probs;
+    int32_t* len_hist;
+    int32_t* dev_error;
+    RowStat* stats;  // target rows [B*(k+1)], then draft rows [B*k]
+};
+
+__device__ __forceinline__ int tgt_row(const LinearArgs& a, int b, int i) { return b * (a.k + 1) + i; }
+__device__ __forceinline__ int drf_row(const LinearArgs& a, int b, int i) { return a.B * (a.k + 1) + b * a.k + i; }
+
+// One CTA per row (persistent).  MODE 0 greedy, 1 sampled, 2 sampled + top-p.
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kNT, 1) k_linear_rowstats(LinearArgs a) {
+    extern __shared__ uint4 dyn_smem[];
+    __shared__ BlockScratch s;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(dyn_smem);
+    const int nt = a.B * (a.k + 1);
+    const int R = nt + (MODE > 0 ? a.B * a.k : 0);
+    const T* tgt = static_cast<const T*>(a.tgt);
+    const T* drf = static_cast<const T*>(a.drf);
+    for (int r = blockIdx.x; r < R; r += gridDim.x) {
+        const T* row;
+        int tok;
+        if (r < nt) {
+            const int b = r / (a.k + 1), i = r - b * (a.k + 1);
+            row = tgt + (size_t)r * a.V;
+            tok = (i < a.k) ? a.drafts[(size_t)b * a.k + i] : -1;
+        } else {
+            const int rr = r - nt;
+            row = drf + (size_t)rr * a.V;
+            tok = a.drafts[rr];
+        }
+        const RowStat st = row_stats<T, MODE>(row, a.V, a.c, a.top_p, tok, hist, s);
+        if (threadIdx.x == 0) a.stats[r] = st;
+        __syncthreads();
+    }
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kNT, 1) k_linear_finalize(LinearArgs a) {
+    __shared__ BlockScratch s;
+    __shared__ SampleScratch ss;
+    __shared__ int sh_a, sh_inval;
+    constexpr int VEC = ElemT<T>::VEC;
+    const int b = blockIdx.x, k = a.k, V = a.V;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t req = a.req ? a.req[b] : (int64_t)b;
+    const int64_t pos = a.pos ? a.pos[b] : 0;
+    const int32_t* d = a.drafts + (size_t)b * k;
+
+    if (warp == 0) {
+        int inval = 0;
+        for (int i = lane; i <= k; i += 32)
+            if (a.stats[tgt_row(a, b, i)].flags & kRowInvalid) inval |= kDevErrNonfinite;
+        if (MODE > 0)
+            for (int i = lane; i < k; i += 32)
+                if (a.stats[drf_row(a, b, i)].flags & kRowInvalid) inval |= kDevErrNonfinite;
+        for (int i = lane; i < k; i += 32)
+            if (d[i] < 0 || d[i] >= V) inval |= kDevErrToken;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) inval |= __shfl_xor_sync(0xffffffffu, inval, o);
+        int first_reject = k;
+        for (int i0 = 0; i0 < k; i0 += 32) {
+            const int i = i0 + lane;
+            bool acc = true;
+            float ap = 0.0f, pp = 0.0f, qq = 0.0f;
+            if (i < k && !inval) {
+                const RowStat sp = a.stats[tgt_row(a, b, i)];
+                if (MODE == 0) {
+                    acc = (d[i] == sp.argmax);
+                    ap = acc ? 1.0f : 0.0f;
+                    pp = ap;
+                    qq = 1.0f;
+                } else {
+                    const RowStat sq = a.stats[drf_row(a, b, i)];
+                    pp = (sp.flags & kRowTokMember) ? weight_of(sp.x_tok, a.c, scaled_max(sp.m, a.c)) * sp.inv_zn : 0.0f;
+                    qq = (sq.flags & kRowTokMember) ? weight_of(sq.x_tok, a.c, scaled_max(sq.m, a.c)) * sq.inv_zn : 0.0f;
+                    const float ratio = qq > 0.0f ? pp / qq : 0.0f;
+                    ap = fminf(1.0f, ratio);
+                    acc = uniform01(a.seed, req, pos + i + 1, kPurposeAccept, 0) < ratio;
+                }
+            }
+            if (i < k) {
+                if (a.accept_prob) a.accept_prob[(size_t)b * k + i] = inval ? 0.0f : ap;
+                if (a.token_probs) {
+                    a.token_probs[((size_t)b * k + i) * 2 + 0] = inval ? 0.0f : pp;
+                    a.token_probs[((size_t)b * k + i) * 2 + 1] = inval ? 0.0f : qq;
+                }
+            }
+            const unsigned rej = __ballot_sync(0xffffffffu, i < k && !acc);
+            if (rej && first_reject == k) first_reject = i0 + __ffs(rej) - 1;
+        }
+        if (lane == 0) {
+            sh_a = inval ? 0 : first_reject;
+            sh_inval = inval;
+        }
+    }
+    __syncthreads();
+    const int acnt = sh_a, inval = sh_inval;
+    const T* tgt = static_cast<const T*>(a.tgt) + (size_t)b * (k + 1) * V;
+    int t;
+    if (inval) {
+        t = row_argmax_finite<T>(tgt, V, s);
+    } else if (MODE == 0) {
+        t = a.stats[tgt_row(a, b, acnt)].argmax;
+    } else {
+        const RowStat sp = a.stats[tgt_row(a, b, acnt)];
+        const T* prow = tgt + (size_t)acnt * V;
+        const RowView<T> rv(prow, V);
+        const FilteredRow<T> P(prow, sp, a.c, nucleus_cut<T>(prow, V, sp, s));
+        const bool resid = acnt < k;
+        const float u = uniform01(a.seed, req, pos + acnt + 1, resid ? kPurposeResidual : kPurposeBonus, 0);
+        auto wp = [&](int unit, float* w, int& i0, int& cnt) {
+            rv.unit_range(unit, i0, cnt);
+            P.probs(i0, cnt, w);
+        };
+        if (resid) {
+            const RowStat sq = a.stats[drf_row(a, b, acnt)];
+            const T* qrow = static_cast<const T*>(a.drf) + ((size_t)b * k + acnt) * V;
+            const FilteredRow<T> Q(qrow, sq, a.c, nucleus_cut<T>(qrow, V, sq, s));
+            auto wr = [&](int unit, float* w, int& i0, int& cnt) {
+                rv.unit_range(unit, i0, cnt);
+                float q[VEC];
+                P.probs(i0, cnt, w);
+                Q.probs(i0, cnt, q);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) w[j] = fmaxf(0.0f, w[j] - q[j]);
+            };
+            t = block_inverse_cdf<VEC>(rv.units(), u, wr, s, ss);
+            if (t < 0) t = block_inverse_cdf<VEC>(rv.units(), u, wp, s, ss);
+        } else {
+            t = block_inverse_cdf<VEC>(rv.units(), u, wp, s, ss);
+        }
+    }
+    if (threadIdx.x == 0) {
+        a.acc_len[b] = acnt;
+        int32_t* o = a.out_tokens + (size_t)b * (k + 1);
+        for (int j = 0; j <= k; ++j) o[j] = (j < acnt) ? d[j] : (j == acnt ? t : -1);
+        if (a.len_hist) atomicAdd(a.len_hist + acnt, 1);
+        if (inval && a.dev_error) atomicOr(a.dev_error, inval);
+    }
+}
+
+template <typename T, int MODE>
+static spec_status launch_linear(LinearArgs& a, cudaStream_t st) {
+    const int nt = a.B * (a.k + 1);
+    const int R = nt + (MODE > 0 ? a.B * a.k : 0);
+    const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kHistBins * 4 : 0;
+    auto* k1 = k_linear_rowstats<T, MODE>;
+    int grid = 0;
+    if (!launch_grid(k1, dyn, R, &grid)) return SPEC_ERR_CUDA;
+    k1<<<grid, kNT, dyn, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    k_linear_finalize<T, MODE><<<a.B, kNT, 0, st>>>(a);
+    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" spec_status spec_verify_linear(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                          const int32_t* draft_tokens, int B, int k, int V,
+                                          const int64_t* request_ids, const int64_t* positions,
+                                          const spec_sampling_params* params, int32_t* accepted_len,
+                                          int32_t* out_tokens, float* accept_prob, float* token_probs,
+                                          int32_t* len_hist, int32_t* dev_error, void* workspace,
+                                          size_t workspace_bytes, spec_stream_t stream) {
+    if (!params || !target_logits || !draft_tokens || !accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
+    if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
+    if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+    if (k > 64) return SPEC_ERR_UNSUPPORTED;
+    const float T = params->temperature, top_p = params->top_p;
+    if (!(T >= 0.0f) || !(T < INFINITY) || !(top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;
+    const bool greedy = (T == 0.0f);
+    if (!greedy && !draft_logits) return SPEC_ERR_INVALID_ARG;
+    if ((int64_t)V > kMaxTiles * (int64_t)kNT * 4 - 16) return SPEC_ERR_UNSUPPORTED;
+    if ((int64_t)B * (2 * k + 1) > 0x7fffffffLL / 2) return SPEC_ERR_UNSUPPORTED;
+    const size_t need = spec_workspace_size(SPEC_OP_LINEAR, B, k, V, dtype);
+    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return SPEC_ERR_WORKSPACE;
+    if (!select_device_of(target_logits)) return SPEC_ERR_INVALID_ARG;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (len_hist && cudaMemsetAsync(len_hist, 0, sizeof(int32_t) * (size_t)(k + 1), st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    LinearArgs a;
+    a.tgt = target_logits;
+    a.drf = draft_logits;
+    a.drafts = draft_tokens;
+    a.B = B; a.k = k; a.V = V;
+    a.req = request_ids;
+    a.pos = positions;
+    a.T = T;
+    a.top_p = top_p;
+    a.c = greedy ? 0.0f : (float)(1.4426950408889634 / (double)T);
+    a.seed = params->seed;
+    a.acc_len = accepted_len;
+    a.out_tokens = out_tokens;
+    a.accept_prob = accept_prob;
+    a.token_probs = token_probs;
+    a.len_hist = len_hist;
+    a.dev_error = dev_error;
+    a.stats = static_cast<RowStat*>(workspace);
+    const int mode = greedy ? 0 : (top_p < 1.0f ? 2 : 1);
+    if (dtype == SPEC_BF16) {
+        if (mode == 0) return launch_linear<__nv_bfloat16, 0>(a, st);
+        if (mode == 1) return launch_linear<__nv_bfloat16, 1>(a, st);
+        return launch_linear<__nv_bfloat16, 2>(a, st);
+    }
+    if (mode == 0) return launch_linear<float, 0>(a, st);
+    if (mode == 1) return launch_linear<float, 1>(a, st);
+    return launch_linear<float, 2>(a, st);
+}

@@ -1,0 +1,91 @@
+"""The C-ABI library builds, loads, and exports every function declared in
+include/specverify.h; host-side argument checks reject bad calls before any
+CUDA work (these run without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_verification_60_gb300 import build
+
+    build.build()
+    import speculative_decoding_verification_60_gb300 as svp
+
+    return svp.load()
+
+
+def _declared():
+    names = []
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(spec_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert set(declared) >= {"spec_verify_linear", "spec_verify_tree", "spec_compact_accepted",
+                             "spec_workspace_size", "spec_status_string"}
+    for name in declared:
+        assert hasattr(lib, name), name
+    import speculative_decoding_verification_60_gb300 as svp
+
+    assert set(svp.EXPORTS) == set(declared)
+
+
+def test_status_strings(lib):
+    import speculative_decoding_verification_60_gb300 as svp
+
+    assert svp.status_string(0) == "SPEC_OK"
+    assert svp.status_string(3) == "SPEC_ERR_WORKSPACE"
+    assert svp.status_string(99) == "SPEC_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(lib):
+    import speculative_decoding_verification_60_gb300 as svp
+
+    assert svp.workspace_size(svp.SPEC_OP_LINEAR, 256, 8, 128256) >= 256 * 17 * 32
+    assert svp.workspace_size(svp.SPEC_OP_LINEAR, 0, 8, 128256) == 0
+    assert svp.workspace_size(svp.SPEC_OP_TREE, 32, 60, 128256) > 0
+
+
+def test_host_argument_checks_return_status(lib):
+    from speculative_decoding_verification_60_gb300 import SamplingParams
+
+    sp = SamplingParams(1.0, 1.0, 0, 0)
+    dummy = ctypes.c_void_p(16)
+    # no params / null logits / bad sizes / bad temperature: rejected before any CUDA call
+    assert lib.spec_verify_linear(dummy, dummy, 0, dummy, 1, 1, 8, None, None, None, dummy, dummy,
+                                  None, None, None, None, dummy, 1 << 20, None) == 1
+    assert lib.spec_verify_linear(None, dummy, 0, dummy, 1, 1, 8, None, None, ctypes.byref(sp), dummy, dummy,
+                                  None, None, None, None, dummy, 1 << 20, None) == 1
+    assert lib.spec_verify_linear(dummy, dummy, 0, dummy, 0, 1, 8, None, None, ctypes.byref(sp), dummy, dummy,
+                                  None, None, None, None, dummy, 1 << 20, None) == 1
+    bad = SamplingParams(-1.0, 1.0, 0, 0)
+    assert lib.spec_verify_linear(dummy, dummy, 0, dummy, 1, 1, 8, None, None, ctypes.byref(bad), dummy, dummy,
+                                  None, None, None, None, dummy, 1 << 20, None) == 1
+    assert lib.spec_verify_linear(dummy, dummy, 0, dummy, 1, 65, 8, None, None, ctypes.byref(sp), dummy, dummy,
+                                  None, None, None, None, dummy, 1 << 20, None) == 2
+    assert lib.spec_verify_linear(dummy, dummy, 0, dummy, 1, 1, 8, None, None, ctypes.byref(sp), dummy, dummy,
+                                  None, None, None, None, dummy, 8, None) == 3
+    assert lib.spec_verify_tree(dummy, dummy, 0, dummy, dummy, 1, 3, 8, 3, None, None, ctypes.byref(sp),
+                                dummy, dummy, dummy, None, dummy, 256, None) == 1
+    assert lib.spec_compact_accepted(None, 1, 1, 8, dummy, None, dummy, 1, dummy, dummy, dummy, None, None) == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import speculative_decoding_verification_60_gb300._binding as b
+
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not found"):
+        b.load()
