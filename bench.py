@@ -1,0 +1,488 @@
+#!/usr/bin/env python3
+"""Benchmark of libspecverify on GB300.
+
+A step is one pass of the verification hot path over one batch of the
+top-p workload (B=256 requests, k=8 drafts, V=128256, bf16 logits,
+temperature 0.7, top-p 0.9): per-row statistics of all 2k+1 rows of every
+request, the accept tests with the residual / bonus draw, and the
+compaction of the accepted positions' hidden rows (H=7168) for the next
+draft step.  The tree path (B=32, 60-node top-4 tree of depth 5) is timed
+beside it.  Inputs are synthetic (seeded) and larger than L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank verifies its own
+batch (requests are independent: weak scaling, no collective on the data
+path); the step time is the max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "linear-b256-k8-v128256-t0.7-p0.9"
+TREE_WORKLOAD = "tree-b32-n60-k4-d5-v128256"
+HIDDEN = 7168
+METRIC = "verified logit rows/s at V=128256 bf16; achieved HBM GB/s vs GB300 peak"
+UNIT = "rows/s"
+PROFILE = os.path.join(ROOT, "profiles", "k_linear_rowstats_linear-b256-k8-v128256-t0.7-p0.9.md")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-requests", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs on a smaller batch)")
+    ap.add_argument("--no-tree", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def source_sha() -> str:
+    """Hash of the kernel sources, to tell whether recorded counters still apply."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_60_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(f.encode())
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the row-statistics kernel from the committed
+    ncu summary, or None when that summary is missing or was taken on other
+    kernel sources."""
+    if not os.path.exists(PROFILE):
+        return None
+    kv = {}
+    for line in open(PROFILE):
+        if ":" in line and line.strip().startswith("- "):
+            key, _, val = line.strip()[2:].partition(":")
+            kv[key.strip()] = val.strip().strip("`")
+    if kv.get("source_sha") != source_sha():
+        return None
+    try:
+        return float(kv["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        return float(json.load(open(p))["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def draft_tokens_torch(drf, T: float, top_p: float, seed: int, chunk: int = 256):
+    """Synthetic draft tokens: one draw per draft row from its filtered
+    softmax (the draft model's own sampling; input generation only)."""
+    import torch
+
+    B, k, V = drf.shape
+    flat = drf.reshape(B * k, V)
+    g = torch.Generator(device=drf.device)
+    g.manual_seed(seed)
+    out = torch.empty(B * k, dtype=torch.int64, device=drf.device)
+    for r0 in range(0, B * k, chunk):
+        x = flat[r0:r0 + chunk].float() / T
+        p = torch.softmax(x, dim=-1)
+        if top_p < 1.0:
+            ps, idx = torch.sort(p, dim=-1, descending=True, stable=True)
+            keep = (torch.cumsum(ps, dim=-1) - ps) < top_p
+            ps = ps * keep
+            p = torch.zeros_like(p).scatter_(1, idx, ps)
+        out[r0:r0 + chunk] = torch.multinomial(p, 1, generator=g).squeeze(1)
+    return out.reshape(B, k).to(torch.int32)
+
+
+class LinearStep:
+    """Device-resident inputs, outputs and workspace of one rank's batch,
+    and the raw C-ABI calls of one step."""
+
+    def __init__(self, rank: int, device, batch=None):
+        import torch
+
+        import speculative_decoding_verification_60_gb300 as svp
+        import synth
+
+        self.torch = torch
+        self.svp = svp
+        self.lib = svp.load()
+        w = synth.WORKLOADS[WORKLOAD]
+        self.B, self.k, self.V = (batch or w["B"]), w["k"], w["V"]
+        self.T, self.top_p, self.seed = w["T"], w["top_p"], w["seed"]
+        B, k, V = self.B, self.k, self.V
+        self.dev = device
+        self.tgt, self.drf = synth.linear_logits(B, k, V, "bf16", w["data_seed"] + 97 * rank, device=device)
+        self.d = draft_tokens_torch(self.drf, self.T, self.top_p, seed=11 + rank)
+        self.req = (torch.arange(B, dtype=torch.int64, device=device) + rank * B)
+        self.pos = torch.full((B,), 1000, dtype=torch.int64, device=device)
+        self.hidden = synth.hidden_states(B, k + 1, HIDDEN, seed=w["data_seed"] + 1 + rank, device=device)
+        ws = svp.workspace_size(svp.SPEC_OP_LINEAR, B, k, V)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        i32, f32 = torch.int32, torch.float32
+        self.acc = torch.empty(B, dtype=i32, device=device)
+        self.toks = torch.empty(B, k + 1, dtype=i32, device=device)
+        self.aprob = torch.empty(B, k, dtype=f32, device=device)
+        self.tprob = torch.empty(B, k, 2, dtype=f32, device=device)
+        self.hist = torch.empty(k + 1, dtype=i32, device=device)
+        self.err = torch.empty(1, dtype=i32, device=device)
+        self.ohid = torch.empty(B * (k + 1), HIDDEN, dtype=torch.bfloat16, device=device)
+        self.offs = torch.empty(B + 1, dtype=i32, device=device)
+        self.ntok = torch.empty(B * (k + 1), dtype=i32, device=device)
+        self.cerr = torch.empty(1, dtype=i32, device=device)
+        self.sp = svp.SamplingParams(self.T, self.top_p, self.seed, 0)
+        self.algo_bytes = B * (2 * k + 1) * V * 2  # one read of every target and draft row
+
+    @staticmethod
+    def P(t):
+        return ctypes.c_void_p(t.data_ptr())
+
+    def stats(self, stream):
+        P = self.P
+        st = self.lib.spec_linear_stats(P(self.tgt), P(self.drf), 0, P(self.d), self.B, self.k, self.V,
+                                        ctypes.byref(self.sp), P(self.ws), self.ws.numel(),
+                                        ctypes.c_void_p(stream.cuda_stream))
+        assert st == 0, self.svp.status_string(st)
+
+    def decide(self, stream):
+        P = self.P
+        st = self.lib.spec_linear_decide(P(self.tgt), P(self.drf), 0, P(self.d), self.B, self.k, self.V, P(self.req),
+                                         P(self.pos), ctypes.byref(self.sp), P(self.acc), P(self.toks), P(self.aprob),
+                                         P(self.tprob), P(self.hist), P(self.err), P(self.ws), self.ws.numel(),
+                                         ctypes.c_void_p(stream.cuda_stream))
+        assert st == 0, self.svp.status_string(st)
+
+    def verify(self, stream):
+        P = self.P
+        st = self.lib.spec_verify_linear(P(self.tgt), P(self.drf), 0, P(self.d), self.B, self.k, self.V, P(self.req),
+                                         P(self.pos), ctypes.byref(self.sp), P(self.acc), P(self.toks), P(self.aprob),
+                                         P(self.tprob), P(self.hist), P(self.err), P(self.ws), self.ws.numel(),
+                                         ctypes.c_void_p(stream.cuda_stream))
+        assert st == 0, self.svp.status_string(st)
+
+    def compact(self, stream):
+        P = self.P
+        st = self.lib.spec_compact_accepted(P(self.hidden), self.B, self.k + 1, HIDDEN, P(self.acc), None,
+                                            P(self.toks), self.k + 1, P(self.ohid), P(self.offs), P(self.ntok),
+                                            P(self.cerr), ctypes.c_void_p(stream.cuda_stream))
+        assert st == 0, self.svp.status_string(st)
+
+
+def time_linear(step: LinearStep, K: int, W: int, barrier):
+    """K timed steps after W warm-up steps, on one stream; returns
+    (ms per step, mean ms of the row-statistics launch, launches)."""
+    torch = step.torch
+    s = torch.cuda.current_stream()
+    for _ in range(W):
+        step.stats(s)
+        step.decide(s)
+        step.compact(s)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for i in range(K):
+        ev[i][0].record(s)
+        step.stats(s)
+        ev[i][1].record(s)
+        step.decide(s)
+        step.compact(s)
+    e1.record(s)
+    torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1) / K
+    stats_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return ms, stats_ms, 3 * K
+
+
+def time_e2e(step: LinearStep, K: int):
+    """The same step through the public calls with host buffers: per step
+    the inputs are copied from pinned host memory, verified, compacted, and
+    the accepted lengths and tokens copied back."""
+    torch = step.torch
+    s = torch.cuda.current_stream()
+    hosts = [step.tgt.cpu().pin_memory(), step.drf.cpu().pin_memory(), step.d.cpu().pin_memory(),
+             step.hidden.cpu().pin_memory()]
+    devs = [step.tgt, step.drf, step.d, step.hidden]
+    outs = [step.acc, step.toks]
+    outs_h = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+    h2d = sum(h.numel() * h.element_size() for h in hosts)
+    d2h = sum(o.numel() * o.element_size() for o in outs)
+
+    def one():
+        for h, d in zip(hosts, devs):
+            d.copy_(h, non_blocking=True)
+        step.verify(s)
+        step.compact(s)
+        for o, oh in zip(outs, outs_h):
+            oh.copy_(o, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(K):
+        one()
+    e1.record(s)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / K, h2d, d2h
+
+
+def time_tree(device, K: int, W: int):
+    import numpy as np
+    import torch
+
+    import speculative_decoding_verification_60_gb300 as svp
+    import synth
+
+    w = synth.WORKLOADS[TREE_WORKLOAD]
+    B, N, V = w["B"], w["N"], w["V"]
+    parent = synth.pruned_tree(w["K"], w["depth"], N)
+    tgt, drf = synth.tree_logits(B, N, V, w["data_seed"], device=device)
+    # node tokens: each child drawn from its parent's draft row (input generation only)
+    tok = torch.zeros(B, N, dtype=torch.int32, device=device)
+    par = torch.as_tensor(parent, dtype=torch.long, device=device)
+    flat = drf[:, par[1:]].reshape(B * (N - 1), V).float() / w["T"]
+    tok[:, 1:] = torch.multinomial(torch.softmax(flat, -1), 1).reshape(B, N - 1).to(torch.int32)
+    parent_d = torch.as_tensor(parent, dtype=torch.int32, device=device)
+    out = None
+    for _ in range(W):
+        out = svp.verify_tree(tgt, drf, tok, parent_d, w["depth"], w["T"], w["top_p"], w["seed"], svp.CHILD_IID)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(K):
+        out = svp.verify_tree(tgt, drf, tok, parent_d, w["depth"], w["T"], w["top_p"], w["seed"], svp.CHILD_IID)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / K
+    acc = out["accepted_len"].cpu().numpy()
+    return {"workload": TREE_WORKLOAD, "ms_per_step": round(ms, 4), "requests": B,
+            "verified_nodes_per_s": round(B * N / (ms / 1e3), 1), "mean_accepted_depth": float(np.mean(acc)),
+            "child_mode": "iid"}
+
+
+def cpu_baseline(step: LinearStep, n_req: int) -> dict:
+    """The oracle, as it stands, on a bounded sample (n_req requests) of the
+    same batch, single-threaded on the host."""
+    import oracle
+
+    sel = list(range(n_req))
+    tgt = step.tgt[sel].cpu()
+    drf = step.drf[sel].cpu()
+    d = step.d[sel].cpu().numpy()
+    req = step.req[sel].cpu().numpy()
+    pos = step.pos[sel].cpu().numpy()
+    t0 = time.perf_counter()
+    for b in range(n_req):  # one request at a time, as the method defines it
+        oracle.verify_linear(tgt[b:b + 1], drf[b:b + 1], d[b:b + 1], step.T, step.top_p, step.seed,
+                             req_ids=req[b:b + 1], positions=pos[b:b + 1])
+    dt = time.perf_counter() - t0
+    return {"value": round(n_req * (step.k + 1) / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n_req} of {step.B} requests of {WORKLOAD} ({n_req * (2 * step.k + 1)} rows), "
+                      f"fp64 C oracle, {dt:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, local_rank, world = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    step = LinearStep(rank, device, args.batch)
+    clocks = Clocks(local_rank)
+    clocks.start()
+    ms, stats_ms, launches = time_linear(step, args.steps, args.warmup, barrier)
+    clk = clocks.stop()
+    if world > 1:
+        t = torch.tensor([ms, stats_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, stats_ms = float(t[0]), float(t[1])
+    rows = step.B * (step.k + 1) * world
+    value = rows / (ms / 1e3)
+    e2e_ms, h2d, d2h = (ms, 0, 0) if args.no_e2e else time_e2e(step, args.e2e_steps)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+    tree = None if args.no_tree else time_tree(device, max(3, args.steps // 2), 2)
+    peak, peak_kind = hbm_peak()
+    achieved = step.algo_bytes / (stats_ms / 1e3) / 1e9
+    acc = step.acc.cpu()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD if args.batch is None else f"{WORKLOAD} (B={step.B})", "B": step.B, "k": step.k, "V": step.V, "temperature": step.T,
+                   "top_p": step.top_p, "hidden": HIDDEN, "rows_per_step": step.B * (2 * step.k + 1),
+                   "l2": "inputs larger than L2 (1116 MB of logits per step, L2 129 MB)",
+                   "parallelism": f"dp{world} (independent request shards)" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "kernel": "k_linear_rowstats", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_kind": peak_kind, "traffic": recorded_traffic(),
+                     "algorithmic_bytes_per_launch": step.algo_bytes, "launch_ms": round(stats_ms, 4)},
+        "e2e": {"value": round(rows / (e2e_ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "mean_accepted_len": round(float(acc.float().mean()), 4),
+        "tree": tree,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(step, args.cpu_requests)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    """The reference arm: the oracle, as it stands, on the host cores; each
+    step is one request of the same workload."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+
+    import oracle
+    import synth
+
+    w = synth.WORKLOADS[WORKLOAD]
+    k, V, T, top_p = w["k"], w["V"], w["T"], w["top_p"]
+    n = args.warmup + args.steps
+    tgt, drf = synth.linear_logits(n, k, V, "bf16", w["data_seed"])
+    d = np.zeros((n, k), dtype=np.int32)
+    for b in range(n):
+        d[b] = oracle.sample_rows(drf[b], T, top_p, seed=11, req=np.full(k, b), pos=np.arange(k))
+    times = []
+    for b in range(n):
+        t0 = time.perf_counter()
+        oracle.verify_linear(tgt[b:b + 1], drf[b:b + 1], d[b:b + 1], T, top_p, w["seed"],
+                             req_ids=np.array([b]), positions=np.array([1000]))
+        if b >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    ms = 1e3 * statistics.mean(times)
+    value = (k + 1) / (ms / 1e3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": 1, "k": k, "V": V, "temperature": T, "top_p": top_p,
+                   "note": "each step one request of the workload"},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} requests of {WORKLOAD}, one per step, fp64 C oracle"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

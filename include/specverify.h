@@ -144,6 +144,28 @@ spec_status spec_verify_linear(const void* target_logits, const void* draft_logi
                                void* workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /*
+ * The two stages of spec_verify_linear, for callers that want to start the
+ * streaming pass as soon as the logits exist or to time it on its own:
+ * spec_linear_stats reads every target row (and every draft row when
+ * T > 0) once and writes per-row statistics into `workspace`;
+ * spec_linear_decide reads them back, runs the accept tests and the
+ * residual / bonus draw, and writes the outputs.  Called in that order on
+ * one stream with identical inputs, params and workspace, they give exactly
+ * the results of spec_verify_linear (which is these two calls).  The
+ * workspace must not be reused between them.  Arguments as above.
+ */
+spec_status spec_linear_stats(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                              const int32_t* draft_tokens, int B, int k, int V,
+                              const spec_sampling_params* params, void* workspace, size_t workspace_bytes,
+                              spec_stream_t stream);
+spec_status spec_linear_decide(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                               const int32_t* draft_tokens, int B, int k, int V,
+                               const int64_t* request_ids, const int64_t* positions,
+                               const spec_sampling_params* params, int32_t* accepted_len, int32_t* out_tokens,
+                               float* accept_prob, float* token_probs, int32_t* len_hist, int32_t* dev_error,
+                               const void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
  * Tree verification (section "EAGLE": a static draft tree explored with the
  * Top-K candidates of every node; the longest accepted root-to-leaf path is
  * kept plus one target token).

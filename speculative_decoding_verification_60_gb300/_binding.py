@@ -23,8 +23,8 @@ CHILD_WOR, CHILD_IID, CHILD_DETERMINISTIC = 0, 1, 2
 DEVERR_TOKEN, DEVERR_NONFINITE, DEVERR_PARENT, DEVERR_LENGTH = 1, 2, 4, 8
 
 # Every symbol declared in include/specverify.h.
-EXPORTS = ("spec_workspace_size", "spec_verify_linear", "spec_verify_tree", "spec_compact_accepted",
-           "spec_status_string")
+EXPORTS = ("spec_workspace_size", "spec_verify_linear", "spec_linear_stats", "spec_linear_decide",
+           "spec_verify_tree", "spec_compact_accepted", "spec_status_string")
 
 
 class SamplingParams(ctypes.Structure):
@@ -56,6 +56,11 @@ def load() -> ctypes.CDLL:
     lib.spec_verify_linear.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams),
                                        P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_linear.restype = I
+    lib.spec_linear_stats.argtypes = [P, P, I, P, I, I, I, ctypes.POINTER(SamplingParams), P, Z, P]
+    lib.spec_linear_stats.restype = I
+    lib.spec_linear_decide.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams),
+                                       P, P, P, P, P, P, P, Z, P]
+    lib.spec_linear_decide.restype = I
     lib.spec_verify_tree.argtypes = [P, P, I, P, P, I, I, I, I, P, P, ctypes.POINTER(SamplingParams),
                                      P, P, P, P, P, Z, P]
     lib.spec_verify_tree.restype = I

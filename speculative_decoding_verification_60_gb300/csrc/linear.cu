@@ -162,8 +162,9 @@ __global__ void __launch_bounds__(kNT, 1) k_linear_finalize(LinearArgs a) {
     }
 }
 
+// Stage 1: statistics of every target and draft row into the workspace.
 template <typename T, int MODE>
-static spec_status launch_linear(LinearArgs& a, cudaStream_t st) {
+static spec_status launch_stats(LinearArgs& a, cudaStream_t st) {
     const int nt = a.B * (a.k + 1);
     const int R = nt + (MODE > 0 ? a.B * a.k : 0);
     const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kHistBins * 4 : 0;
@@ -171,24 +172,34 @@ static spec_status launch_linear(LinearArgs& a, cudaStream_t st) {
     int grid = 0;
     if (!launch_grid(k1, dyn, R, &grid)) return SPEC_ERR_CUDA;
     k1<<<grid, kNT, dyn, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-    k_linear_finalize<T, MODE><<<a.B, kNT, 0, st>>>(a);
-    if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
-    return SPEC_OK;
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
-}  // namespace sv
+// Stage 2: accept tests, accepted length and the residual / bonus draw.
+template <typename T, int MODE>
+static spec_status launch_decide(LinearArgs& a, cudaStream_t st) {
+    k_linear_finalize<T, MODE><<<a.B, kNT, 0, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
 
-using namespace sv;
+template <typename T>
+static spec_status launch_stage(LinearArgs& a, int mode, int stage, cudaStream_t st) {
+    if (stage == 0) {
+        if (mode == 0) return launch_stats<T, 0>(a, st);
+        if (mode == 1) return launch_stats<T, 1>(a, st);
+        return launch_stats<T, 2>(a, st);
+    }
+    if (mode == 0) return launch_decide<T, 0>(a, st);
+    if (mode == 1) return launch_decide<T, 1>(a, st);
+    return launch_decide<T, 2>(a, st);
+}
 
-extern "C" spec_status spec_verify_linear(const void* target_logits, const void* draft_logits, spec_dtype dtype,
-                                          const int32_t* draft_tokens, int B, int k, int V,
-                                          const int64_t* request_ids, const int64_t* positions,
-                                          const spec_sampling_params* params, int32_t* accepted_len,
-                                          int32_t* out_tokens, float* accept_prob, float* token_probs,
-                                          int32_t* len_hist, int32_t* dev_error, void* workspace,
-                                          size_t workspace_bytes, spec_stream_t stream) {
-    if (!params || !target_logits || !draft_tokens || !accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
+// Host-side checks shared by the linear entry points; fills `a` and `mode`.
+static spec_status prepare_linear(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                  const int32_t* draft_tokens, int B, int k, int V, const int64_t* request_ids,
+                                  const int64_t* positions, const spec_sampling_params* params, void* workspace,
+                                  size_t workspace_bytes, LinearArgs& a, int& mode) {
+    if (!params || !target_logits || !draft_tokens) return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
     if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
     if (k > 64) return SPEC_ERR_UNSUPPORTED;
@@ -202,11 +213,7 @@ extern "C" spec_status spec_verify_linear(const void* target_logits, const void*
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return SPEC_ERR_WORKSPACE;
     if (!select_device_of(target_logits)) return SPEC_ERR_INVALID_ARG;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (len_hist && cudaMemsetAsync(len_hist, 0, sizeof(int32_t) * (size_t)(k + 1), st) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-    LinearArgs a;
+    a = LinearArgs{};
     a.tgt = target_logits;
     a.drf = draft_logits;
     a.drafts = draft_tokens;
@@ -217,20 +224,81 @@ extern "C" spec_status spec_verify_linear(const void* target_logits, const void*
     a.top_p = top_p;
     a.c = greedy ? 0.0f : (float)(1.4426950408889634 / (double)T);
     a.seed = params->seed;
+    a.stats = static_cast<RowStat*>(workspace);
+    mode = greedy ? 0 : (top_p < 1.0f ? 2 : 1);
+    return SPEC_OK;
+}
+
+static spec_status run_stage(LinearArgs& a, spec_dtype dtype, int mode, int stage, cudaStream_t st) {
+    return dtype == SPEC_BF16 ? launch_stage<__nv_bfloat16>(a, mode, stage, st) : launch_stage<float>(a, mode, stage, st);
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" spec_status spec_verify_linear(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                          const int32_t* draft_tokens, int B, int k, int V,
+                                          const int64_t* request_ids, const int64_t* positions,
+                                          const spec_sampling_params* params, int32_t* accepted_len,
+                                          int32_t* out_tokens, float* accept_prob, float* token_probs,
+                                          int32_t* len_hist, int32_t* dev_error, void* workspace,
+                                          size_t workspace_bytes, spec_stream_t stream) {
+    if (!accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
+    LinearArgs a;
+    int mode = 0;
+    spec_status r = prepare_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
+                                   params, workspace, workspace_bytes, a, mode);
+    if (r != SPEC_OK) return r;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (len_hist && cudaMemsetAsync(len_hist, 0, sizeof(int32_t) * (size_t)(k + 1), st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
     a.acc_len = accepted_len;
     a.out_tokens = out_tokens;
     a.accept_prob = accept_prob;
     a.token_probs = token_probs;
     a.len_hist = len_hist;
     a.dev_error = dev_error;
-    a.stats = static_cast<RowStat*>(workspace);
-    const int mode = greedy ? 0 : (top_p < 1.0f ? 2 : 1);
-    if (dtype == SPEC_BF16) {
-        if (mode == 0) return launch_linear<__nv_bfloat16, 0>(a, st);
-        if (mode == 1) return launch_linear<__nv_bfloat16, 1>(a, st);
-        return launch_linear<__nv_bfloat16, 2>(a, st);
-    }
-    if (mode == 0) return launch_linear<float, 0>(a, st);
-    if (mode == 1) return launch_linear<float, 1>(a, st);
-    return launch_linear<float, 2>(a, st);
+    r = run_stage(a, dtype, mode, 0, st);
+    if (r != SPEC_OK) return r;
+    return run_stage(a, dtype, mode, 1, st);
+}
+
+extern "C" spec_status spec_linear_stats(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                         const int32_t* draft_tokens, int B, int k, int V,
+                                         const spec_sampling_params* params, void* workspace, size_t workspace_bytes,
+                                         spec_stream_t stream) {
+    LinearArgs a;
+    int mode = 0;
+    const spec_status r = prepare_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, nullptr, nullptr,
+                                         params, workspace, workspace_bytes, a, mode);
+    if (r != SPEC_OK) return r;
+    return run_stage(a, dtype, mode, 0, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" spec_status spec_linear_decide(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                          const int32_t* draft_tokens, int B, int k, int V,
+                                          const int64_t* request_ids, const int64_t* positions,
+                                          const spec_sampling_params* params, int32_t* accepted_len,
+                                          int32_t* out_tokens, float* accept_prob, float* token_probs,
+                                          int32_t* len_hist, int32_t* dev_error, const void* workspace,
+                                          size_t workspace_bytes, spec_stream_t stream) {
+    if (!accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
+    LinearArgs a;
+    int mode = 0;
+    spec_status r = prepare_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
+                                   params, const_cast<void*>(workspace), workspace_bytes, a, mode);
+    if (r != SPEC_OK) return r;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (len_hist && cudaMemsetAsync(len_hist, 0, sizeof(int32_t) * (size_t)(k + 1), st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    a.acc_len = accepted_len;
+    a.out_tokens = out_tokens;
+    a.accept_prob = accept_prob;
+    a.token_probs = token_probs;
+    a.len_hist = len_hist;
+    a.dev_error = dev_error;
+    return run_stage(a, dtype, mode, 1, st);
 }
