@@ -166,6 +166,31 @@ spec_status spec_linear_decide(const void* target_logits, const void* draft_logi
                                const void* workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /*
+ * spec_verify_linear for callers that cannot allocate device memory at the
+ * point where they verify (code inside a custom allocator or memory pool,
+ * code whose device memory is fixed at start-up, code that only receives
+ * buffers from a host framework).  The page describes no such variant; it
+ * exists for those callers only.
+ *
+ * Same arguments and results as spec_verify_linear, without the workspace:
+ * the per-row statistics go to a fixed 2 MiB array inside the library's
+ * device image, which every GPU that loads the library keeps until the
+ * process exits.  Limits: B * (2k + 1) <= 65536 rows, else
+ * SPEC_ERR_UNSUPPORTED (nothing is enqueued).  The call allocates nothing
+ * (no cudaMalloc, cudaFree or allocating library routine).  The first call
+ * on each device looks up the array's device address once; make that first
+ * call before any stream capture.  Every call shares the one array, so
+ * calls that overlap on the GPU (different streams or host threads) race on
+ * it; each call writes every row it later reads, so no state carries over.
+ */
+spec_status spec_verify_linear_noalloc(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                       const int32_t* draft_tokens, int B, int k, int V,
+                                       const int64_t* request_ids, const int64_t* positions,
+                                       const spec_sampling_params* params, int32_t* accepted_len,
+                                       int32_t* out_tokens, float* accept_prob, float* token_probs,
+                                       int32_t* len_hist, int32_t* dev_error, spec_stream_t stream);
+
+/*
  * Tree verification (section "EAGLE": a static draft tree explored with the
  * Top-K candidates of every node; the longest accepted root-to-leaf path is
  * kept plus one target token).

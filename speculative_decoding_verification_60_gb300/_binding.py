@@ -24,7 +24,7 @@ DEVERR_TOKEN, DEVERR_NONFINITE, DEVERR_PARENT, DEVERR_LENGTH = 1, 2, 4, 8
 
 # Every symbol declared in include/specverify.h.
 EXPORTS = ("spec_workspace_size", "spec_verify_linear", "spec_linear_stats", "spec_linear_decide",
-           "spec_verify_tree", "spec_compact_accepted", "spec_status_string")
+           "spec_verify_linear_noalloc", "spec_verify_tree", "spec_compact_accepted", "spec_status_string")
 
 
 class SamplingParams(ctypes.Structure):
@@ -61,6 +61,9 @@ def load() -> ctypes.CDLL:
     lib.spec_linear_decide.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams),
                                        P, P, P, P, P, P, P, Z, P]
     lib.spec_linear_decide.restype = I
+    lib.spec_verify_linear_noalloc.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams),
+                                               P, P, P, P, P, P, P]
+    lib.spec_verify_linear_noalloc.restype = I
     lib.spec_verify_tree.argtypes = [P, P, I, P, P, I, I, I, I, P, P, ctypes.POINTER(SamplingParams),
                                      P, P, P, P, P, Z, P]
     lib.spec_verify_tree.restype = I

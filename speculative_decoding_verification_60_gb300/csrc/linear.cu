@@ -2,6 +2,8 @@
 // §Speculative decoding and §Target-Draft): row statistics of every target
 // and draft row, then per request the accept tests, the accepted length
 // and the residual or bonus draw.
+#include <mutex>
+
 #include "../../include/specverify.h"
 #include "launch.cuh"
 #include "sample.cuh"
@@ -301,4 +303,64 @@ extern "C" spec_status spec_linear_decide(const void* target_logits, const void*
     a.len_hist = len_hist;
     a.dev_error = dev_error;
     return run_stage(a, dtype, mode, 1, st);
+}
+
+// ---------------------------------------------------------------------------
+// Variant of spec_verify_linear that allocates nothing and takes no
+// workspace.  Some callers cannot allocate device memory when they verify:
+// code running inside a custom allocator or memory pool, code that must not
+// grow its memory after start-up, or code whose buffers are all handed to it
+// by a host framework.  This variant keeps the per-row statistics in a
+// fixed array that lives in the library's device image, so the caller only
+// passes inputs and outputs.
+//
+// The array holds kNoAllocMaxRows rows (2 MiB); every GPU that loads the
+// library keeps it until the process exits.  Calls with B * (2k + 1) rows
+// above that limit return SPEC_ERR_UNSUPPORTED.  All calls share the array,
+// so calls that overlap on the GPU (on different streams, or from different
+// host threads) race on it.  Each call writes every row's statistics before
+// reading them, so nothing in the array needs to start at zero.
+// ---------------------------------------------------------------------------
+namespace sv {
+
+constexpr int kNoAllocMaxRows = 65536;
+static __device__ __align__(256) RowStat g_noalloc_stats[kNoAllocMaxRows];
+
+constexpr int kNoAllocMaxDevices = 64;
+static std::mutex g_noalloc_mutex;
+static void* g_noalloc_ptr[kNoAllocMaxDevices];
+
+// Device address of the array on the current device.  The first call on a
+// device resolves it (once), so make that first call before any stream
+// capture begins.
+static spec_status noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return SPEC_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_stats) != cudaSuccess || !p) return SPEC_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return SPEC_OK;
+}
+
+}  // namespace sv
+
+extern "C" spec_status spec_verify_linear_noalloc(const void* target_logits, const void* draft_logits,
+                                                  spec_dtype dtype, const int32_t* draft_tokens, int B, int k, int V,
+                                                  const int64_t* request_ids, const int64_t* positions,
+                                                  const spec_sampling_params* params, int32_t* accepted_len,
+                                                  int32_t* out_tokens, float* accept_prob, float* token_probs,
+                                                  int32_t* len_hist, int32_t* dev_error, spec_stream_t stream) {
+    if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
+    if ((int64_t)B * (2 * (int64_t)k + 1) > kNoAllocMaxRows) return SPEC_ERR_UNSUPPORTED;
+    if (!target_logits || !select_device_of(target_logits)) return SPEC_ERR_INVALID_ARG;
+    void* scratch = nullptr;
+    const spec_status r = noalloc_scratch(&scratch);
+    if (r != SPEC_OK) return r;
+    return spec_verify_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
+                              params, accepted_len, out_tokens, accept_prob, token_probs, len_hist, dev_error,
+                              scratch, sizeof(RowStat) * (size_t)kNoAllocMaxRows, stream);
 }
