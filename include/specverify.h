@@ -31,7 +31,11 @@
  *    Shaw, SC'11): key = (seed lo32, seed hi32), counter = (request lo32,
  *    position lo32, purpose | round << 8, request hi32), u = (word0 >> 8) *
  *    2^-24.  Results depend only on (inputs, seed, request id, position),
- *    never on the batch size or on a request's slot in the batch.
+ *    not on the batch size or on a request's slot in the batch: bit for bit
+ *    when every row starts on a 16-byte boundary (V * element size a
+ *    multiple of 16 and 16-byte aligned base pointers); otherwise rows in
+ *    different slots are summed in a different order, and only decisions
+ *    that sit within rounding of a threshold can differ.
  *  - Calls that overlap on the GPU must not share output or workspace
  *    buffers.
  */

@@ -11,7 +11,7 @@
 
 namespace sv {
 
-constexpr int kNT = 1024;            // threads of every row-level CTA
+constexpr int kNT = 512;             // threads of every row-level CTA
 constexpr int kNW = kNT / 32;        // warps of such a CTA
 constexpr int kPurposeAccept = 1;
 constexpr int kPurposeResidual = 2;
@@ -99,6 +99,16 @@ struct BlockScratch {
     double bcast_d[4];
     float bcast_f[8];
     int bcast_i[8];
+    float ffh[kNW];
+    float ffl[kNW];
+    float ffh2[kNW + 1];
+    float ffl2[kNW + 1];
+    // per-warp results of the fused row reduction (used by nothing else)
+    float red_m[kNW];
+    float red_zh[kNW];
+    float red_zl[kNW];
+    int red_i[kNW];
+    int red_b[kNW];
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -120,6 +130,32 @@ __device__ __forceinline__ double warp_sum_d(double v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// ------------------------------------------------- float-float arithmetic --
+// FP64 runs at a small fraction of the FP32 rate on this GPU, so sums that
+// must carry more than 24 bits across a block are kept as unevaluated pairs
+// hi + lo of floats, combined with error-free two-sums (Knuth).
+struct ff {
+    float hi, lo;
+};
+__device__ __forceinline__ ff ff_from(float x) { return ff{x, 0.0f}; }
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    const float s = a.hi + b.hi;
+    const float bb = s - a.hi;
+    const float e = (a.hi - (s - bb)) + (b.hi - bb);
+    const float t = e + a.lo + b.lo;
+    const float h = s + t;
+    return ff{h, t - (h - s)};
+}
+__device__ __forceinline__ ff ff_add_f(ff a, float b) { return ff_add(a, ff{b, 0.0f}); }
+__device__ __forceinline__ ff ff_scale(ff a, float f) { return ff{a.hi * f, a.lo * f}; }
+__device__ __forceinline__ double ff_to_double(ff a) { return (double)a.hi + (double)a.lo; }
+__device__ __forceinline__ ff ff_shfl_xor(ff v, int o) {
+    return ff{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
+    return ff{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
 }
 
 // All threads of the CTA must call these (they contain __syncthreads).
@@ -159,37 +195,65 @@ __device__ __forceinline__ int block_sum_i(int v, BlockScratch& s) {
 __device__ __forceinline__ bool block_any(bool v, BlockScratch& s) {
     return __syncthreads_or(v ? 1 : 0) != 0;
 }
-// Deterministic fp64 sum: fixed shuffle tree, then warp totals in order.
-__device__ __forceinline__ double block_sum_d(double v, BlockScratch& s) {
+// Deterministic block sum in float-float: fixed shuffle tree, then warp
+// totals in order; every thread gets the same result.
+__device__ __forceinline__ ff block_sum_ff(ff v, BlockScratch& s) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    v = warp_sum_d(v);
-    if (lane == 0) s.d[w] = v;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
+    if (lane == 0) { s.ffh[w] = v.hi; s.ffl[w] = v.lo; }
     __syncthreads();
-    double r = 0.0;
-#pragma unroll 4
-    for (int i = 0; i < kNW; ++i) r += s.d[i];
+    ff r = ff{s.ffh[0], s.ffl[0]};
+    for (int i = 1; i < kNW; ++i) r = ff_add(r, ff{s.ffh[i], s.ffl[i]});
     __syncthreads();
     return r;
 }
-// Exclusive prefix in thread order (fp64); *total receives the sum.
-__device__ __forceinline__ double block_exclusive_scan_d(double v, BlockScratch& s, double* total) {
+__device__ __forceinline__ double block_sum_d(double v, BlockScratch& s) {
+    const float hi = (float)v;
+    return ff_to_double(block_sum_ff(ff{hi, (float)(v - (double)hi)}, s));
+}
+// Exclusive prefix in thread order (float-float); *total receives the sum.
+// Warp 0 turns the warp totals into exclusive prefixes once.
+__device__ __forceinline__ ff block_exclusive_scan_ff(ff v, BlockScratch& s, ff* total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    double x = v;
+    ff x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        const ff y = ff_shfl_up(x, o);
+        if (lane >= o) x = ff_add(x, y);
     }
-    if (lane == 31) s.d[w] = x;
+    if (lane == 31) { s.ffh[w] = x.hi; s.ffl[w] = x.lo; }
     __syncthreads();
-    double base = 0.0, tot = 0.0;
-    for (int i = 0; i < kNW; ++i) {
-        if (i < w) base += s.d[i];
-        tot += s.d[i];
+    if (w == 0) {
+        ff t = (lane < kNW) ? ff{s.ffh[lane], s.ffl[lane]} : ff{0.0f, 0.0f};
+        ff incl = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const ff y = ff_shfl_up(incl, o);
+            if (lane >= o) incl = ff_add(incl, y);
+        }
+        const ff tot = ff{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
+        if (lane < kNW) {  // exclusive prefix of warp `lane`
+            const ff ex = ff_add(incl, ff{-t.hi, -t.lo});
+            s.ffh2[lane] = ex.hi;
+            s.ffl2[lane] = ex.lo;
+        }
+        if (lane == 0) { s.ffh2[kNW] = tot.hi; s.ffl2[kNW] = tot.lo; }
     }
     __syncthreads();
-    if (total) *total = tot;
-    return base + x - v;
+    const ff base = ff{s.ffh2[w], s.ffl2[w]};
+    if (total) *total = ff{s.ffh2[kNW], s.ffl2[kNW]};
+    const ff own_neg = ff{-v.hi, -v.lo};
+    const ff r = ff_add(base, ff_add(x, own_neg));
+    __syncthreads();
+    return r;
+}
+__device__ __forceinline__ double block_exclusive_scan_d(double v, BlockScratch& s, double* total) {
+    const float hi = (float)v;
+    ff t;
+    const ff r = block_exclusive_scan_ff(ff{hi, (float)(v - (double)hi)}, s, &t);
+    if (total) *total = ff_to_double(t);
+    return ff_to_double(r);
 }
 __device__ __forceinline__ int block_exclusive_scan_i(int v, BlockScratch& s, int* total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;

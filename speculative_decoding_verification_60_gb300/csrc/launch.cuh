@@ -28,12 +28,12 @@ inline int sm_count() {
 // Persistent grid: min(work, SMs * resident CTAs per SM).  Sets the
 // kernel's dynamic shared-memory limit first when it exceeds the default.
 template <typename K>
-inline bool launch_grid(K kernel, size_t dyn_smem, long long work, int* grid) {
+inline bool launch_grid(K kernel, size_t dyn_smem, long long work, int* grid, int block = 512) {
     if (dyn_smem > 48 * 1024 &&
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) != cudaSuccess)
         return false;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 1024, dyn_smem) != cudaSuccess) return false;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, dyn_smem) != cudaSuccess) return false;
     const int sms = sm_count();
     if (per_sm < 1 || sms < 1) return false;
     long long g = (long long)sms * per_sm;

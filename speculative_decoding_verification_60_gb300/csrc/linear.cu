@@ -33,10 +33,10 @@ __device__ __forceinline__ int drf_row(const LinearArgs& a, int b, int i) { retu
 
 // One CTA per row (persistent).  MODE 0 greedy, 1 sampled, 2 sampled + top-p.
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kNT, 1) k_linear_rowstats(LinearArgs a) {
+__global__ void __launch_bounds__(kNT, 2) k_linear_rowstats(LinearArgs a) {
     extern __shared__ uint4 dyn_smem[];
     __shared__ BlockScratch s;
-    uint32_t* hist = reinterpret_cast<uint32_t*>(dyn_smem);
+    uint8_t* topsmem = reinterpret_cast<uint8_t*>(dyn_smem);
     const int nt = a.B * (a.k + 1);
     const int R = nt + (MODE > 0 ? a.B * a.k : 0);
     const T* tgt = static_cast<const T*>(a.tgt);
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kNT, 1) k_linear_rowstats(LinearArgs a) {
             row = drf + (size_t)rr * a.V;
             tok = a.drafts[rr];
         }
-        const RowStat st = row_stats<T, MODE>(row, a.V, a.c, a.top_p, tok, hist, s);
+        const RowStat st = row_stats<T, MODE>(row, a.V, a.c, a.top_p, tok, topsmem, s);
         if (threadIdx.x == 0) a.stats[r] = st;
         __syncthreads();
     }
@@ -169,10 +169,10 @@ template <typename T, int MODE>
 static spec_status launch_stats(LinearArgs& a, cudaStream_t st) {
     const int nt = a.B * (a.k + 1);
     const int R = nt + (MODE > 0 ? a.B * a.k : 0);
-    const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kHistBins * 4 : 0;
+    const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kTopSmemBytes : 0;
     auto* k1 = k_linear_rowstats<T, MODE>;
     int grid = 0;
-    if (!launch_grid(k1, dyn, R, &grid)) return SPEC_ERR_CUDA;
+    if (!launch_grid(k1, dyn, R, &grid, kNT)) return SPEC_ERR_CUDA;
     k1<<<grid, kNT, dyn, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }

@@ -37,8 +37,8 @@ __device__ int block_inverse_cdf(int units, float u, const WeightFn& wf, BlockSc
             for (int j = 0; j < VEC; ++j)
                 if (j < cnt) acc += w[j];
         }
-        const double ts = block_sum_d((double)acc, s);
-        if (threadIdx.x == 0) ss.tile[t] = ts;
+        const ff ts = block_sum_ff(ff_from(acc), s);
+        if (threadIdx.x == 0) ss.tile[t] = ff_to_double(ts);
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -81,8 +81,7 @@ __device__ int block_inverse_cdf(int units, float u, const WeightFn& wf, BlockSc
         for (int j = 0; j < VEC; ++j)
             if (j < cnt) acc += w[j];
     }
-    double tot;
-    const double before = pre + block_exclusive_scan_d((double)acc, s, &tot);
+    const double before = pre + ff_to_double(block_exclusive_scan_ff(ff_from(acc), s, nullptr));
     if (threadIdx.x == 0) { s.bcast_i[5] = 0x7fffffff; s.bcast_i[6] = -1; }
     __syncthreads();
     int last_pos = -1;
@@ -113,7 +112,7 @@ __device__ int block_inverse_cdf(int units, float u, const WeightFn& wf, BlockSc
 // Sum over a row of a per-unit weight function (fp64, deterministic).
 template <int VEC, typename WeightFn>
 __device__ double block_weight_total(int units, const WeightFn& wf, BlockScratch& s) {
-    double acc = 0.0;
+    ff acc = ff{0.0f, 0.0f};
     for (int unit = threadIdx.x; unit < units; unit += kNT) {
         float w[VEC];
         int i0, cnt;
@@ -122,9 +121,9 @@ __device__ double block_weight_total(int units, const WeightFn& wf, BlockScratch
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
             if (j < cnt) a += w[j];
-        acc += (double)a;
+        acc = ff_add_f(acc, a);
     }
-    return block_sum_d(acc, s);
+    return ff_to_double(block_sum_ff(acc, s));
 }
 
 // Filtered probabilities of a filtered row over an index range of at most

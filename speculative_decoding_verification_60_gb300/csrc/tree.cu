@@ -33,20 +33,21 @@ struct TreeArgs {
 
 // State of the rejected rounds at the current node.
 struct Rounds {
-    int n;                      // rounds rejected so far
-    int tok[kMaxChildren];      // rejected token of each round
-    double norm[kMaxChildren];  // IID/WOR: residual mass N_i;  DET: 1 - P_i(x_i)
-    float qscale[kMaxChildren]; // WOR: 1 / (1 - Q_i(x_i)), 0 when that mass is 1
+    int n;                        // rounds rejected so far
+    int tok[kMaxChildren];        // rejected token of each round
+    float inv_norm[kMaxChildren]; // 1 / (IID/WOR: residual mass N_i;  DET: 1 - P_i(x_i)); 0 => P unchanged
+    float qscale[kMaxChildren];   // WOR: 1 / (1 - Q_i(x_i)), 0 when that mass is 1
 };
 
 // P_j(v), Q_j(v) after the recorded rejected rounds, from the filtered
 // probabilities p, q of token v.
 __device__ __forceinline__ void chain(float& P, float& Q, int v, const Rounds& R, int mode) {
     for (int i = 0; i < R.n; ++i) {
+        const float in = R.inv_norm[i];
         if (mode == SPEC_CHILD_DETERMINISTIC) {
-            P = (v == R.tok[i]) ? 0.0f : (R.norm[i] > 0.0 ? (float)((double)P / R.norm[i]) : P);
+            P = (v == R.tok[i]) ? 0.0f : (in > 0.0f ? P * in : P);
         } else {
-            P = R.norm[i] > 0.0 ? (float)((double)fmaxf(0.0f, P - Q) / R.norm[i]) : P;
+            P = in > 0.0f ? fmaxf(0.0f, P - Q) * in : P;
             if (mode == SPEC_CHILD_WOR) Q = (v == R.tok[i]) ? 0.0f : Q * R.qscale[i];
         }
     }
@@ -55,7 +56,7 @@ __device__ __forceinline__ void chain(float& P, float& Q, int v, const Rounds& R
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
     extern __shared__ uint4 dyn_smem[];
-    uint32_t* hist = reinterpret_cast<uint32_t*>(dyn_smem);
+    uint8_t* topsmem = reinterpret_cast<uint8_t*>(dyn_smem);
     __shared__ BlockScratch s;
     __shared__ SampleScratch ss;
     __shared__ Rounds R;
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
         }
         const int m = sh_m;
         const T* prow = tgt + (size_t)n * V;
-        const RowStat sp = row_stats<T, MODE>(prow, V, a.c, a.top_p, -1, hist, s);
+        const RowStat sp = row_stats<T, MODE>(prow, V, a.c, a.top_p, -1, topsmem, s);
         if (sp.flags & kRowInvalid) {
             if (tid == 0) atomicOr(&sh_inval, kDevErrNonfinite);
             inval = true;
@@ -163,7 +164,7 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
         RowStat sq = sp;
         const T* qrow = drf ? drf + (size_t)n * V : prow;
         if (use_q) {
-            sq = row_stats<T, MODE>(qrow, V, a.c, a.top_p, -1, hist, s);
+            sq = row_stats<T, MODE>(qrow, V, a.c, a.top_p, -1, topsmem, s);
             if (sq.flags & kRowInvalid) {
                 if (tid == 0) atomicOr(&sh_inval, kDevErrNonfinite);
                 inval = true;
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
                 const float u = uniform01(a.seed, req, pos + dep + 1, kPurposeAccept, j);
                 sh_next = (u < ratio) ? ch[j] : -1;
                 R.tok[j] = x;
-                if (a.mode == SPEC_CHILD_DETERMINISTIC) R.norm[j] = 1.0 - (double)Px;
+                if (a.mode == SPEC_CHILD_DETERMINISTIC) R.inv_norm[j] = (Px < 1.0f) ? 1.0f / (1.0f - Px) : 0.0f;
                 R.qscale[j] = (Qx < 1.0f) ? 1.0f / (1.0f - Qx) : 0.0f;
             }
             __syncthreads();
@@ -206,7 +207,7 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
                     }
                 };
                 const double Nj = block_weight_total<VEC>(rv.units(), wres, s);
-                if (tid == 0) R.norm[j] = Nj;
+                if (tid == 0) R.inv_norm[j] = Nj > 0.0 ? (float)(1.0 / Nj) : 0.0f;
             }
             if (tid == 0) R.n = j + 1;
             __syncthreads();
@@ -253,7 +254,7 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
 
 template <typename T, int MODE>
 static spec_status launch_tree(TreeArgs& a, cudaStream_t st) {
-    const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kHistBins * 4 : 0;
+    const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kTopSmemBytes : 0;
     auto* k = k_tree<T, MODE>;
     if (!set_dyn_smem(k, dyn)) return SPEC_ERR_CUDA;
     k<<<a.B, kNT, dyn, st>>>(a);
