@@ -11,7 +11,7 @@
 
 namespace sv {
 
-constexpr int kNT = 512;             // threads of every row-level CTA
+constexpr int kNT = 256;             // threads of every row-level CTA
 constexpr int kNW = kNT / 32;        // warps of such a CTA
 constexpr int kPurposeAccept = 1;
 constexpr int kPurposeResidual = 2;
@@ -91,24 +91,24 @@ __device__ __forceinline__ uint32_t bf16_bits_round_down(float f) {
 }
 
 // ------------------------------------------------------- block reductions --
+// Every block-wide operation below follows one pattern: per-warp partials
+// are published, one barrier, warp 0 merges them in a fixed order and
+// publishes the result, a second barrier, every thread reads the result.
+// Partials and results live in different slots, so no trailing barrier is
+// needed: the next operation's warp 0 writes a result only after that
+// operation's first barrier, which every reader of the previous result has
+// passed.
 struct BlockScratch {
-    double d[kNW];
-    float f[kNW];
-    int i[kNW];
-    unsigned u[kNW];
-    double bcast_d[4];
-    float bcast_f[8];
+    float pf[kNW];        // per-warp float partials
+    float pf2[kNW];       // second float partial (float-float low parts)
+    float pf3[kNW];
+    int pi[kNW];          // per-warp int partials
+    int pi2[kNW];
+    float rf[kNW + 2];    // results: floats (scans: per-warp prefixes + total)
+    float rf2[kNW + 2];
+    int ri[kNW + 2];      // results: ints
+    float bcast_f[8];     // free-form broadcast slots (callers own the barriers)
     int bcast_i[8];
-    float ffh[kNW];
-    float ffl[kNW];
-    float ffh2[kNW + 1];
-    float ffl2[kNW + 1];
-    // per-warp results of the fused row reduction (used by nothing else)
-    float red_m[kNW];
-    float red_zh[kNW];
-    float red_zl[kNW];
-    int red_i[kNW];
-    int red_b[kNW];
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -126,16 +126,12 @@ __device__ __forceinline__ int warp_sum_i(int v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
 
 // ------------------------------------------------- float-float arithmetic --
 // FP64 runs at a small fraction of the FP32 rate on this GPU, so sums that
-// must carry more than 24 bits across a block are kept as unevaluated pairs
-// hi + lo of floats, combined with error-free two-sums (Knuth).
+// must carry more than 24 bits are kept as unevaluated pairs hi + lo of
+// floats, combined with error-free transformations (Knuth's two-sum,
+// Dekker's product through fma).
 struct ff {
     float hi, lo;
 };
@@ -149,130 +145,149 @@ __device__ __forceinline__ ff ff_add(ff a, ff b) {
     return ff{h, t - (h - s)};
 }
 __device__ __forceinline__ ff ff_add_f(ff a, float b) { return ff_add(a, ff{b, 0.0f}); }
+__device__ __forceinline__ ff ff_neg(ff a) { return ff{-a.hi, -a.lo}; }
+__device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, ff_neg(b)); }
 __device__ __forceinline__ ff ff_scale(ff a, float f) { return ff{a.hi * f, a.lo * f}; }
-__device__ __forceinline__ double ff_to_double(ff a) { return (double)a.hi + (double)a.lo; }
+// a * b exactly, as a pair
+__device__ __forceinline__ ff ff_two_prod(float a, float b) {
+    const float p = a * b;
+    return ff{p, fmaf(a, b, -p)};
+}
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+    const ff p = ff_two_prod(a.hi, b);
+    const float lo = fmaf(a.lo, b, p.lo);
+    const float h = p.hi + lo;
+    return ff{h, lo - (h - p.hi)};
+}
+__device__ __forceinline__ float ff_to_float(ff a) { return a.hi + a.lo; }
+// a >= b, decided on the pair difference (its sign is the sign of hi, or of
+// lo when hi is zero)
+__device__ __forceinline__ bool ff_ge(ff a, ff b) {
+    const ff d = ff_sub(a, b);
+    return d.hi > 0.0f || (d.hi == 0.0f && d.lo >= 0.0f);
+}
+__device__ __forceinline__ bool ff_lt(ff a, ff b) { return !ff_ge(a, b); }
 __device__ __forceinline__ ff ff_shfl_xor(ff v, int o) {
     return ff{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
 }
 __device__ __forceinline__ ff ff_shfl_up(ff v, int o) {
     return ff{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
 }
-
-// All threads of the CTA must call these (they contain __syncthreads).
-__device__ __forceinline__ float block_max(float v, BlockScratch& s) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    v = warp_max(v);
-    if (lane == 0) s.f[w] = v;
-    __syncthreads();
-    float r = s.f[0];
-#pragma unroll 4
-    for (int i = 1; i < kNW; ++i) r = fmaxf(r, s.f[i]);
-    __syncthreads();
-    return r;
+__device__ __forceinline__ ff ff_shfl(ff v, int src) {
+    return ff{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
 }
-__device__ __forceinline__ int block_min_i(int v, BlockScratch& s) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    v = warp_min_i(v);
-    if (lane == 0) s.i[w] = v;
-    __syncthreads();
-    int r = s.i[0];
-#pragma unroll 4
-    for (int i = 1; i < kNW; ++i) r = min(r, s.i[i]);
-    __syncthreads();
-    return r;
-}
-__device__ __forceinline__ int block_sum_i(int v, BlockScratch& s) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    v = warp_sum_i(v);
-    if (lane == 0) s.i[w] = v;
-    __syncthreads();
-    int r = 0;
-#pragma unroll 4
-    for (int i = 0; i < kNW; ++i) r += s.i[i];
-    __syncthreads();
-    return r;
-}
-__device__ __forceinline__ bool block_any(bool v, BlockScratch& s) {
-    return __syncthreads_or(v ? 1 : 0) != 0;
-}
-// Deterministic block sum in float-float: fixed shuffle tree, then warp
-// totals in order; every thread gets the same result.
-__device__ __forceinline__ ff block_sum_ff(ff v, BlockScratch& s) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+__device__ __forceinline__ ff warp_sum_ff(ff v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
-    if (lane == 0) { s.ffh[w] = v.hi; s.ffl[w] = v.lo; }
-    __syncthreads();
-    ff r = ff{s.ffh[0], s.ffl[0]};
-    for (int i = 1; i < kNW; ++i) r = ff_add(r, ff{s.ffh[i], s.ffl[i]});
-    __syncthreads();
-    return r;
+    return v;
 }
-__device__ __forceinline__ double block_sum_d(double v, BlockScratch& s) {
-    const float hi = (float)v;
-    return ff_to_double(block_sum_ff(ff{hi, (float)(v - (double)hi)}, s));
-}
-// Exclusive prefix in thread order (float-float); *total receives the sum.
-// Warp 0 turns the warp totals into exclusive prefixes once.
-__device__ __forceinline__ ff block_exclusive_scan_ff(ff v, BlockScratch& s, ff* total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    ff x = v;
+// Inclusive prefix over the lanes of a warp.
+__device__ __forceinline__ ff warp_inclusive_scan_ff(ff x) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const ff y = ff_shfl_up(x, o);
         if (lane >= o) x = ff_add(x, y);
     }
-    if (lane == 31) { s.ffh[w] = x.hi; s.ffl[w] = x.lo; }
-    __syncthreads();
-    if (w == 0) {
-        ff t = (lane < kNW) ? ff{s.ffh[lane], s.ffl[lane]} : ff{0.0f, 0.0f};
-        ff incl = t;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const ff y = ff_shfl_up(incl, o);
-            if (lane >= o) incl = ff_add(incl, y);
-        }
-        const ff tot = ff{__shfl_sync(0xffffffffu, incl.hi, 31), __shfl_sync(0xffffffffu, incl.lo, 31)};
-        if (lane < kNW) {  // exclusive prefix of warp `lane`
-            const ff ex = ff_add(incl, ff{-t.hi, -t.lo});
-            s.ffh2[lane] = ex.hi;
-            s.ffl2[lane] = ex.lo;
-        }
-        if (lane == 0) { s.ffh2[kNW] = tot.hi; s.ffl2[kNW] = tot.lo; }
-    }
-    __syncthreads();
-    const ff base = ff{s.ffh2[w], s.ffl2[w]};
-    if (total) *total = ff{s.ffh2[kNW], s.ffl2[kNW]};
-    const ff own_neg = ff{-v.hi, -v.lo};
-    const ff r = ff_add(base, ff_add(x, own_neg));
-    __syncthreads();
-    return r;
+    return x;
 }
-__device__ __forceinline__ double block_exclusive_scan_d(double v, BlockScratch& s, double* total) {
-    const float hi = (float)v;
-    ff t;
-    const ff r = block_exclusive_scan_ff(ff{hi, (float)(v - (double)hi)}, s, &t);
-    if (total) *total = ff_to_double(t);
-    return ff_to_double(r);
-}
-__device__ __forceinline__ int block_exclusive_scan_i(int v, BlockScratch& s, int* total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int x = v;
+__device__ __forceinline__ int warp_inclusive_scan_i(int x) {
+    const int lane = threadIdx.x & 31;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, x, o);
         if (lane >= o) x += y;
     }
-    if (lane == 31) s.i[w] = x;
+    return x;
+}
+
+// All threads of the CTA must call these.
+__device__ __forceinline__ float block_max(float v, BlockScratch& s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_max(v);
+    if (lane == 0) s.pf[w] = v;
     __syncthreads();
-    int base = 0, tot = 0;
-    for (int i = 0; i < kNW; ++i) {
-        if (i < w) base += s.i[i];
-        tot += s.i[i];
+    if (w == 0) {
+        float r = warp_max(lane < kNW ? s.pf[lane] : -INFINITY);
+        if (lane == 0) s.rf[0] = r;
     }
     __syncthreads();
-    if (total) *total = tot;
-    return base + x - v;
+    return s.rf[0];
+}
+__device__ __forceinline__ int block_min_i(int v, BlockScratch& s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_min_i(v);
+    if (lane == 0) s.pi[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        const int r = warp_min_i(lane < kNW ? s.pi[lane] : 0x7fffffff);
+        if (lane == 0) s.ri[0] = r;
+    }
+    __syncthreads();
+    return s.ri[0];
+}
+__device__ __forceinline__ int block_sum_i(int v, BlockScratch& s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_sum_i(v);
+    if (lane == 0) s.pi[w] = v;
+    __syncthreads();
+    if (w == 0) {
+        const int r = warp_sum_i(lane < kNW ? s.pi[lane] : 0);
+        if (lane == 0) s.ri[0] = r;
+    }
+    __syncthreads();
+    return s.ri[0];
+}
+__device__ __forceinline__ bool block_any(bool v, BlockScratch& s) {
+    return __syncthreads_or(v ? 1 : 0) != 0;
+}
+// Deterministic block sum in float-float: fixed shuffle trees.
+__device__ __forceinline__ ff block_sum_ff(ff v, BlockScratch& s) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    v = warp_sum_ff(v);
+    if (lane == 0) { s.pf[w] = v.hi; s.pf2[w] = v.lo; }
+    __syncthreads();
+    if (w == 0) {
+        const ff r = warp_sum_ff(lane < kNW ? ff{s.pf[lane], s.pf2[lane]} : ff{0.0f, 0.0f});
+        if (lane == 0) { s.rf[0] = r.hi; s.rf2[0] = r.lo; }
+    }
+    __syncthreads();
+    return ff{s.rf[0], s.rf2[0]};
+}
+// Exclusive prefix in thread order (float-float); *total receives the sum.
+__device__ __forceinline__ ff block_exclusive_scan_ff(ff v, BlockScratch& s, ff* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const ff x = warp_inclusive_scan_ff(v);
+    if (lane == 31) { s.pf[w] = x.hi; s.pf2[w] = x.lo; }
+    __syncthreads();
+    if (w == 0) {
+        const ff t = (lane < kNW) ? ff{s.pf[lane], s.pf2[lane]} : ff{0.0f, 0.0f};
+        const ff incl = warp_inclusive_scan_ff(t);
+        if (lane < kNW) {
+            const ff ex = ff_sub(incl, t);
+            s.rf[lane] = ex.hi;
+            s.rf2[lane] = ex.lo;
+        }
+        if (lane == kNW - 1) { s.rf[kNW] = incl.hi; s.rf2[kNW] = incl.lo; }
+    }
+    __syncthreads();
+    if (total) *total = ff{s.rf[kNW], s.rf2[kNW]};
+    return ff_add(ff{s.rf[w], s.rf2[w]}, ff_sub(x, v));
+}
+__device__ __forceinline__ int block_exclusive_scan_i(int v, BlockScratch& s, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int x = warp_inclusive_scan_i(v);
+    if (lane == 31) s.pi[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        const int t = (lane < kNW) ? s.pi[lane] : 0;
+        const int incl = warp_inclusive_scan_i(t);
+        if (lane < kNW) s.ri[lane] = incl - t;
+        if (lane == kNW - 1) s.ri[kNW] = incl;
+    }
+    __syncthreads();
+    if (total) *total = s.ri[kNW];
+    return s.ri[w] + x - v;
 }
 
 // ------------------------------------------------------------ row access --

@@ -26,10 +26,10 @@ inline int sm_count() {
 }
 
 // Persistent grid: min(work, SMs * resident CTAs per SM).  Sets the
-// kernel's dynamic shared-memory limit first when it exceeds the default.
+// kernel's dynamic shared-memory limit first.
 template <typename K>
 inline bool launch_grid(K kernel, size_t dyn_smem, long long work, int* grid, int block = 512) {
-    if (dyn_smem > 48 * 1024 &&
+    if (dyn_smem > 0 &&
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) != cudaSuccess)
         return false;
     int per_sm = 0;
@@ -42,9 +42,11 @@ inline bool launch_grid(K kernel, size_t dyn_smem, long long work, int* grid, in
     return true;
 }
 
+// Opt in to dyn_smem bytes of dynamic shared memory: static plus dynamic
+// above 48 KiB needs it even when the dynamic part alone is smaller.
 template <typename K>
 inline bool set_dyn_smem(K kernel, size_t dyn_smem) {
-    if (dyn_smem <= 48 * 1024) return true;
+    if (dyn_smem == 0) return true;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) == cudaSuccess;
 }
 

@@ -33,9 +33,10 @@ __device__ __forceinline__ int drf_row(const LinearArgs& a, int b, int i) { retu
 
 // One CTA per row (persistent).  MODE 0 greedy, 1 sampled, 2 sampled + top-p.
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kNT, 2) k_linear_rowstats(LinearArgs a) {
+__global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a) {
     extern __shared__ uint4 dyn_smem[];
     __shared__ BlockScratch s;
+    __shared__ SampleScratch ss;
     uint8_t* topsmem = reinterpret_cast<uint8_t*>(dyn_smem);
     const int nt = a.B * (a.k + 1);
     const int R = nt + (MODE > 0 ? a.B * a.k : 0);
@@ -53,19 +54,23 @@ __global__ void __launch_bounds__(kNT, 2) k_linear_rowstats(LinearArgs a) {
             row = drf + (size_t)rr * a.V;
             tok = a.drafts[rr];
         }
-        const RowStat st = row_stats<T, MODE>(row, a.V, a.c, a.top_p, tok, topsmem, s);
+        const RowStat st = row_stats<T, MODE>(row, a.V, a.c, a.top_p, tok, topsmem, s, ss);
         if (threadIdx.x == 0) a.stats[r] = st;
         __syncthreads();
     }
 }
 
+// One cluster of kDecCluster CTAs per request: every CTA takes the accept
+// decisions (cheap, identical), the draw is split over the cluster, and CTA 0
+// writes the request's outputs.
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kNT, 1) k_linear_finalize(LinearArgs a) {
+__global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
     __shared__ BlockScratch s;
     __shared__ SampleScratch ss;
     __shared__ int sh_a, sh_inval;
-    constexpr int VEC = ElemT<T>::VEC;
-    const int b = blockIdx.x, k = a.k, V = a.V;
+    cg::cluster_group cl = cg::this_cluster();
+    const int rank = (int)cl.block_rank();
+    const int b = blockIdx.x / kDecCluster, k = a.k, V = a.V;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t req = a.req ? a.req[b] : (int64_t)b;
     const int64_t pos = a.pos ? a.pos[b] : 0;
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(kNT, 1) k_linear_finalize(LinearArgs a) {
                     acc = uniform01(a.seed, req, pos + i + 1, kPurposeAccept, 0) < ratio;
                 }
             }
-            if (i < k) {
+            if (i < k && rank == 0) {
                 if (a.accept_prob) a.accept_prob[(size_t)b * k + i] = inval ? 0.0f : ap;
                 if (a.token_probs) {
                     a.token_probs[((size_t)b * k + i) * 2 + 0] = inval ? 0.0f : pp;
@@ -121,41 +126,31 @@ __global__ void __launch_bounds__(kNT, 1) k_linear_finalize(LinearArgs a) {
     __syncthreads();
     const int acnt = sh_a, inval = sh_inval;
     const T* tgt = static_cast<const T*>(a.tgt) + (size_t)b * (k + 1) * V;
-    int t;
+    int t = -1;
     if (inval) {
-        t = row_argmax_finite<T>(tgt, V, s);
+        if (rank == 0) t = row_argmax_finite<T>(tgt, V, s);
     } else if (MODE == 0) {
         t = a.stats[tgt_row(a, b, acnt)].argmax;
     } else {
         const RowStat sp = a.stats[tgt_row(a, b, acnt)];
         const T* prow = tgt + (size_t)acnt * V;
         const RowView<T> rv(prow, V);
-        const FilteredRow<T> P(prow, sp, a.c, nucleus_cut<T>(prow, V, sp, s));
+        FilteredRow<T> P(prow, sp, a.c, 0x7fffffff);
         const bool resid = acnt < k;
         const float u = uniform01(a.seed, req, pos + acnt + 1, resid ? kPurposeResidual : kPurposeBonus, 0);
-        auto wp = [&](int unit, float* w, int& i0, int& cnt) {
-            rv.unit_range(unit, i0, cnt);
-            P.probs(i0, cnt, w);
-        };
         if (resid) {
             const RowStat sq = a.stats[drf_row(a, b, acnt)];
             const T* qrow = static_cast<const T*>(a.drf) + ((size_t)b * k + acnt) * V;
-            const FilteredRow<T> Q(qrow, sq, a.c, nucleus_cut<T>(qrow, V, sq, s));
-            auto wr = [&](int unit, float* w, int& i0, int& cnt) {
-                rv.unit_range(unit, i0, cnt);
-                float q[VEC];
-                P.probs(i0, cnt, w);
-                Q.probs(i0, cnt, q);
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) w[j] = fmaxf(0.0f, w[j] - q[j]);
-            };
-            t = block_inverse_cdf<VEC>(rv.units(), u, wr, s, ss);
-            if (t < 0) t = block_inverse_cdf<VEC>(rv.units(), u, wp, s, ss);
+            FilteredRow<T> Q(qrow, sq, a.c, 0x7fffffff);
+            nucleus_cuts<T>(cl, rv, P, &Q, s, ss);
+            t = draw_filtered<T, true, (MODE == 2)>(cl, rv, P, Q, u, s, ss);
+            if (t < 0) t = draw_filtered<T, false, (MODE == 2)>(cl, rv, P, P, u, s, ss);  // p == q: draw from p
         } else {
-            t = block_inverse_cdf<VEC>(rv.units(), u, wp, s, ss);
+            nucleus_cuts<T>(cl, rv, P, nullptr, s, ss);
+            t = draw_filtered<T, false, (MODE == 2)>(cl, rv, P, P, u, s, ss);
         }
     }
-    if (threadIdx.x == 0) {
+    if (rank == 0 && threadIdx.x == 0) {
         a.acc_len[b] = acnt;
         int32_t* o = a.out_tokens + (size_t)b * (k + 1);
         for (int j = 0; j <= k; ++j) o[j] = (j < acnt) ? d[j] : (j == acnt ? t : -1);
@@ -180,7 +175,7 @@ static spec_status launch_stats(LinearArgs& a, cudaStream_t st) {
 // Stage 2: accept tests, accepted length and the residual / bonus draw.
 template <typename T, int MODE>
 static spec_status launch_decide(LinearArgs& a, cudaStream_t st) {
-    k_linear_finalize<T, MODE><<<a.B, kNT, 0, st>>>(a);
+    k_linear_finalize<T, MODE><<<a.B * kDecCluster, kNT, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -209,7 +204,7 @@ static spec_status prepare_linear(const void* target_logits, const void* draft_l
     if (!(T >= 0.0f) || !(T < INFINITY) || !(top_p > 0.0f)) return SPEC_ERR_INVALID_ARG;
     const bool greedy = (T == 0.0f);
     if (!greedy && !draft_logits) return SPEC_ERR_INVALID_ARG;
-    if ((int64_t)V > kMaxTiles * (int64_t)kNT * 4 - 16) return SPEC_ERR_UNSUPPORTED;
+    if ((int64_t)V > kMaxVocab) return SPEC_ERR_UNSUPPORTED;
     if ((int64_t)B * (2 * k + 1) > 0x7fffffffLL / 2) return SPEC_ERR_UNSUPPORTED;
     const size_t need = spec_workspace_size(SPEC_OP_LINEAR, B, k, V, dtype);
     if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))

@@ -10,41 +10,31 @@
 namespace sv {
 
 constexpr int kUnroll = 8;             // 16-byte vectors in flight per thread
-// Shared memory of a top-p row (bf16): one 64 KiB region, carved as
+// Shared memory of a top-p row (bf16): one region of kTopSmemBytes, carved as
 //   sample  [0, 16 KiB)      bf16 bit patterns of the systematic sample
-//   band    [16, 44 KiB)     counts of the keys inside the bracket: one
-//                            histogram per warp (brackets up to
-//                            kBandBinsWarp keys) or one shared histogram
-//   coarse  [44, 52.25 KiB)  per-warp sample counts of the estimate (u16 pairs)
-//   tmcount [52.25, 53.3 KiB) counts of the thread maxima per coarse bin
-//   tmax    [60, 62 KiB)     each thread's maximum from pass 1
-// and reused whole by the exact full-window fallback.  Per-warp histograms
-// keep same-address shared atomics inside one warp instruction.
-constexpr int kTopSmemBytes = 64 * 1024;
+//   scount  [16, 24 KiB)     sample counts per value bin of the estimate
+//   tcount  [24, 32 KiB)     thread-maximum counts per value bin
+//   wtot    [32, 32.5 KiB)   per-warp prefix totals of the estimate
+//   tmax    [32.5, 33.5 KiB) each thread's maximum from pass 1
+// After the estimate, [0, 32 KiB) holds the key histogram of the exact
+// count (up to kFullBins consecutive bf16 keys).
 constexpr int kSampleCap = 8192;       // sample slots (2 per batch of kUnroll vectors)
-constexpr int kBandBins = 4096;        // widest bracket, in bf16 keys (shared histogram)
-constexpr int kBandBinsWarp = 448;     // widest bracket counted with per-warp histograms
-constexpr int kBandOffset = 16384;
-constexpr int kCoarseOffset = 45056;
-constexpr int kCoarseWords = (257 + 1) / 2;  // 257 u16 counters per warp
-constexpr int kTmCountOffset = kCoarseOffset + kNW * kCoarseWords * 4;
-constexpr int kCoarseBins = 256;       // value-linear bins of the estimate
-constexpr int kFullBins = kTopSmemBytes / 4;  // key window of the fallback histogram
-constexpr int kTmaxOffset = 61440;
-static_assert(kSampleCap * 2 <= kBandOffset, "sample overlaps the bracket histograms");
-static_assert(kBandOffset + kNW * kBandBinsWarp * 4 <= kCoarseOffset, "bracket histograms overlap the estimate");
-static_assert(kBandOffset + kBandBins * 4 <= kCoarseOffset, "shared bracket histogram overlaps the estimate");
-static_assert(kTmCountOffset + (kCoarseBins + 1) * 4 <= kTmaxOffset, "estimate overlaps the thread maxima");
-static_assert(kTmaxOffset + kNT * 4 <= kTopSmemBytes, "thread maxima outside the region");
-// The estimate counts samples per bin (integer atomics, order-free) and
-// weighs each bin in fixed point (w * 2^40, truncated, which only lowers a
-// sum), so every choice made from it is deterministic.
-constexpr double kFix = 1099511627776.0;
-constexpr float kFixF = 1099511627776.0f;
+constexpr int kEstBins = 2048;         // value-linear bins of the estimate
+constexpr int kBinsPerThread = kEstBins / kNT;
+constexpr int kSCountOffset = 16384;
+constexpr int kTCountOffset = kSCountOffset + kEstBins * 4;
+constexpr int kWTotOffset = kTCountOffset + kEstBins * 4;
+constexpr int kTmaxOffset = kWTotOffset + 512;
+constexpr int kTopSmemBytes = kTmaxOffset + kNT * 4;
+constexpr int kFullBins = 8192;        // widest key window counted in one pass
+static_assert(kSampleCap * 2 <= kSCountOffset, "sample overlaps the estimate bins");
+static_assert(kNW * 16 <= 512, "estimate warp totals overlap the thread maxima");
+static_assert(kFullBins * 4 <= kWTotOffset, "histogram overlaps what the estimate still reads");
+static_assert(kEstBins % (4 * kNT) == 0, "whole uint4 groups of bins per thread");
 
 struct Pass1 {
     float m;     // max (NaN-free); -inf if the row has no non-NaN value
-    double z;    // sum of 2^(x*c - m*c) over the row (when requested)
+    ff z;        // sum of 2^(x*c - m*c) over the row (when requested)
     int argmax;  // lowest index holding m
     bool bad;    // a NaN was seen
 };
@@ -126,53 +116,74 @@ __device__ __forceinline__ float batch_weight_sum<float>(const uint4* v, float c
     return acc;
 }
 
-// One block reduction of pass 1's per-thread results: the max, the sum of
-// weights rescaled to it (fp64), the lowest index holding it, and the NaN
-// flag.  Warps merge with shuffles; one barrier publishes the warp results,
-// which every thread then merges in the same order.
+// Merge of two (max, rescaled sum, lowest argmax, NaN) partials.
+struct P1Part {
+    float m;
+    ff z;
+    int idx;
+    int bad;
+};
+template <bool kSum>
+__device__ __forceinline__ P1Part merge_p1(const P1Part& a, const P1Part& b, float c) {
+    P1Part r;
+    r.m = fmaxf(a.m, b.m);
+    if (kSum) {
+        const ff za = (a.m > -INFINITY) ? ff_scale(a.z, ex2((a.m - r.m) * c)) : ff{0.0f, 0.0f};
+        const ff zb = (b.m > -INFINITY) ? ff_scale(b.z, ex2((b.m - r.m) * c)) : ff{0.0f, 0.0f};
+        r.z = ff_add(za, zb);
+    } else {
+        r.z = ff{0.0f, 0.0f};
+    }
+    r.idx = (a.m == b.m) ? min(a.idx, b.idx) : (a.m > b.m ? a.idx : b.idx);
+    r.bad = a.bad | b.bad;
+    return r;
+}
+template <bool kSum>
+__device__ __forceinline__ P1Part shfl_merge_p1(P1Part p, int o, float c) {
+    P1Part q;
+    q.m = __shfl_xor_sync(0xffffffffu, p.m, o);
+    q.z = ff_shfl_xor(p.z, o);
+    q.idx = __shfl_xor_sync(0xffffffffu, p.idx, o);
+    q.bad = __shfl_xor_sync(0xffffffffu, p.bad, o);
+    return merge_p1<kSum>(p, q, c);
+}
+
+// One block reduction of pass 1's per-thread results: shuffle trees within
+// each warp, then warp 0 merges the warp results (fixed order).
 template <bool kSum>
 __device__ __forceinline__ Pass1 reduce_pass1(float m, ff z, int idx, bool bad, float c, BlockScratch& s) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    int nb = bad ? 1 : 0;
+    P1Part p{m, z, idx, bad ? 1 : 0};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, idx, o);
-        nb |= __shfl_xor_sync(0xffffffffu, nb, o);
-        if (kSum) {
-            const ff z2 = ff_shfl_xor(z, o);
-            const float mn = fmaxf(m, m2);
-            const ff a = (m > -INFINITY) ? ff_scale(z, ex2((m - mn) * c)) : ff{0.0f, 0.0f};
-            const ff b = (m2 > -INFINITY) ? ff_scale(z2, ex2((m2 - mn) * c)) : ff{0.0f, 0.0f};
-            z = ff_add(a, b);
-        }
-        idx = (m == m2) ? min(idx, i2) : (m > m2 ? idx : i2);
-        m = fmaxf(m, m2);
-    }
+    for (int o = 16; o > 0; o >>= 1) p = shfl_merge_p1<kSum>(p, o, c);
     if (lane == 0) {
-        s.red_m[w] = m;
-        s.red_zh[w] = z.hi;
-        s.red_zl[w] = z.lo;
-        s.red_i[w] = idx;
-        s.red_b[w] = nb;
+        s.pf[w] = p.m;
+        s.pf2[w] = p.z.hi;
+        s.pf3[w] = p.z.lo;
+        s.pi[w] = p.idx;
+        s.pi2[w] = p.bad;
+    }
+    __syncthreads();
+    if (w == 0) {
+        P1Part q = (lane < kNW) ? P1Part{s.pf[lane], ff{s.pf2[lane], s.pf3[lane]}, s.pi[lane], s.pi2[lane]}
+                                : P1Part{-INFINITY, ff{0.0f, 0.0f}, 0x7fffffff, 0};
+        __syncwarp();
+#pragma unroll
+        for (int o = kNW / 2; o > 0; o >>= 1) q = shfl_merge_p1<kSum>(q, o, c);
+        if (lane == 0) {
+            s.rf[kNW] = q.m;
+            s.rf[kNW + 1] = q.z.hi;
+            s.rf2[kNW] = q.z.lo;
+            s.ri[kNW] = q.idx;
+            s.ri[kNW + 1] = q.bad;
+        }
     }
     __syncthreads();
     Pass1 r;
-    float M = s.red_m[0];
-#pragma unroll 4
-    for (int i = 1; i < kNW; ++i) M = fmaxf(M, s.red_m[i]);
-    ff Z = ff{0.0f, 0.0f};
-    int I = 0x7fffffff, B = 0;
-    for (int i = 0; i < kNW; ++i) {
-        const float mi = s.red_m[i];
-        if (kSum && mi > -INFINITY) Z = ff_add(Z, ff_scale(ff{s.red_zh[i], s.red_zl[i]}, ex2((mi - M) * c)));
-        if (mi == M) I = min(I, s.red_i[i]);
-        B |= s.red_b[i];
-    }
-    r.m = M;
-    r.z = kSum ? ff_to_double(Z) : 0.0;
-    r.argmax = (I == 0x7fffffff) ? 0 : I;
-    r.bad = B != 0;
+    r.m = s.rf[kNW];
+    r.z = ff{s.rf[kNW + 1], s.rf2[kNW]};
+    r.argmax = (s.ri[kNW] == 0x7fffffff) ? 0 : s.ri[kNW];
+    r.bad = s.ri[kNW + 1] != 0;
     return r;
 }
 
@@ -299,460 +310,445 @@ __device__ int row_argmax_finite(const T* __restrict__ row, int V, BlockScratch&
     return any == 0x7fffffff ? 0 : r;
 }
 
-// Index of the n-th (0-based) element, in index order, among those with
-// index < limit that equal `val`; INT_MAX when there are fewer.  *count
-// receives how many such elements were seen (all of them when n is out of
-// reach, which makes this a counter of equals below `limit`).
-template <typename T>
-__device__ int row_find_nth_equal(const T* __restrict__ row, int V, float val, int n, int limit, int* count,
-                                  BlockScratch& s) {
-    constexpr int VEC = ElemT<T>::VEC;
-    const RowView<T> rv(row, V);
-    int seen = 0, found = 0x7fffffff;
-    for (int t0 = 0; t0 < rv.units(); t0 += kNT) {
-        const int u = t0 + threadIdx.x;
-        float f[VEC];
-        int i0 = 0, cnt = 0;
-        if (u < rv.units()) rv.load_unit(u, f, i0, cnt);
-        int mine = 0;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            if (j < cnt && i0 + j < limit && f[j] == val) ++mine;
-        int tot;
-        const int before = block_exclusive_scan_i(mine, s, &tot);
-        if (n >= seen + before && n < seen + before + mine) {
-            int k = n - seen - before;
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                if (j < cnt && i0 + j < limit && f[j] == val) {
-                    if (k == 0) s.bcast_i[0] = i0 + j;
-                    --k;
-                }
-            }
-        }
-        seen += tot;
-        __syncthreads();
-        const bool hit = n < seen;  // uniform across the CTA
-        if (hit) found = s.bcast_i[0];
-        __syncthreads();
-        if (hit) break;
-    }
-    if (count) *count = seen;
-    return found;
+// Step layout of the block-wide searches: the row's units (RowView: head,
+// 16-byte vectors, tail) are cut into steps of kStepUnits consecutive units;
+// warp w owns a contiguous range of steps and lane l takes units l, l + 32,
+// ... of each step, so loads are coalesced and one barrier publishes the
+// per-step results.
+constexpr int kStepUnits = 128;        // 4 units per lane
+constexpr int kMaxSteps = 1024;        // rows of up to kMaxSteps * kStepUnits units
+constexpr long long kMaxRowUnits = (long long)kMaxSteps * kStepUnits;
+// Largest vocabulary the row kernels accept (fp32 rows of 4 elements per unit).
+constexpr long long kMaxVocab = 4 * (kMaxRowUnits - 2);
+
+struct SampleScratch {
+    float sh[kMaxSteps];  // per-step results (float-float sums, or counts)
+    float sl[kMaxSteps];
+};
+
+__device__ __forceinline__ int steps_per_warp(int units) {
+    const int nsteps = (units + kStepUnits - 1) / kStepUnits;
+    return (nsteps + kNW - 1) / kNW;
 }
 
+// Index of the n-th (0-based) element, in index order, among those with
+// index < limit that equal `val`; INT_MAX when there are fewer.  *count
+// receives how many such elements there are.
+template <typename T>
+__device__ int row_find_nth_equal(const T* __restrict__ row, int V, float val, int n, int limit, int* count,
+                                  BlockScratch& s, SampleScratch& ss) {
+    constexpr int VEC = ElemT<T>::VEC;
+    const RowView<T> rv(row, V);
+    const int units = rv.units();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nsteps = (units + kStepUnits - 1) / kStepUnits;
+    const int spw = steps_per_warp(units);
+    int* sc = reinterpret_cast<int*>(ss.sh);
+    auto matches = [&](int unit, int& i0) -> unsigned {  // bit j: element j of the unit matches
+        unsigned msk = 0u;
+        i0 = 0;
+        if (unit < units) {
+            float f[VEC];
+            int cnt;
+            rv.load_unit(unit, f, i0, cnt);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                if (j < cnt && i0 + j < limit && f[j] == val) msk |= 1u << j;
+        }
+        return msk;
+    };
+    for (int st = warp * spw; st < (warp + 1) * spw && st < nsteps; ++st) {
+        int c = 0;
+#pragma unroll
+        for (int g = 0; g < kStepUnits / 32; ++g) {
+            int i0;
+            c += __popc(matches(st * kStepUnits + g * 32 + lane, i0));
+        }
+        c = warp_sum_i(c);
+        if (lane == 0) sc[st] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (nsteps + 31) / 32;
+        int ls = 0;
+        for (int i = 0; i < per; ++i) {
+            const int st = lane * per + i;
+            if (st < nsteps) ls += sc[st];
+        }
+        const int incl = warp_inclusive_scan_i(ls);
+        const int total = __shfl_sync(0xffffffffu, incl, 31);
+        int found = 0x7fffffff;
+        if (n >= 0 && n < total) {
+            const unsigned bal = __ballot_sync(0xffffffffu, incl > n);
+            const int L = __ffs(bal) - 1;
+            int js = -1, pre = 0;
+            if (lane == L) {
+                int run = incl - ls;
+                for (int i = 0; i < per; ++i) {
+                    const int st = lane * per + i;
+                    if (run + sc[st] > n) { js = st; pre = run; break; }
+                    run += sc[st];
+                }
+            }
+            js = __shfl_sync(0xffffffffu, js, L);
+            pre = __shfl_sync(0xffffffffu, pre, L);
+            for (int g = 0; g < kStepUnits / 32 && found == 0x7fffffff; ++g) {
+                int i0;
+                const unsigned msk = matches(js * kStepUnits + g * 32 + lane, i0);
+                const int c = __popc(msk);
+                const int ic = warp_inclusive_scan_i(c);
+                int hit = 0x7fffffff;
+                if (pre + ic > n && pre + ic - c <= n) {
+                    int k = n - (pre + ic - c);
+                    for (int j = 0; j < VEC; ++j) {
+                        if (msk & (1u << j)) {
+                            if (k == 0) { hit = i0 + j; break; }
+                            --k;
+                        }
+                    }
+                }
+                found = warp_min_i(hit);
+                pre += __shfl_sync(0xffffffffu, ic, 31);
+            }
+        }
+        if (lane == 0) {
+            s.bcast_i[5] = total;
+            s.bcast_i[6] = found;
+        }
+    }
+    __syncthreads();
+    const int r = s.bcast_i[6];
+    if (count) *count = s.bcast_i[5];
+    __syncthreads();
+    return r;
+}
 
+// ------------------------------------------------------------------ top-p --
+// Nucleus of a row (the pages' filter, with ties broken by lower index):
+// walking tokens in decreasing logit order, a token is kept while the mass
+// of the tokens before it is below top_p * Z.  All tokens of one logit value
+// share one weight, so the nucleus is a key tau (the boundary value), the
+// number n_keep of tau-valued tokens kept (the lowest-index ones), and the
+// kept mass.
 struct Topp {
-    float tau;     // boundary logit
+    float tau;     // boundary logit (-inf: every token kept)
     int n_keep;    // boundary-valued tokens kept
     int c_tau;     // boundary-valued tokens in the row
-    double mass;   // nucleus mass (weights relative to the max)
-    bool ok;
+    ff mass;       // nucleus mass (weights relative to the max)
 };
 
 // Key of a bf16 value with -0 folded onto +0.
 __device__ __forceinline__ uint32_t value_key(float x) {
     return x == 0.0f ? 0x8000u : okey16(__float_as_uint(x) >> 16);
 }
+__device__ __forceinline__ float key_value(int key) { return bf16_bits_to_float(okey16_to_bits((uint32_t)key)); }
 
-// Walk bins holding counts of consecutive keys from `key_top` downwards
-// (bin i = key key_top - i), starting at mass F0 above the window, and find
-// where the mass reaches pZ.  Bins are split into contiguous per-thread
-// chunks; chunk masses are scanned in fp64.  Returns ok = false when the
-// window ends first (then *F_end holds the mass above the window's bottom).
-__device__ inline Topp scan_key_bins(const uint32_t* hist, int nbins, int key_top, float c, float mc, double F0,
-                                     double pZ, double* F_end, BlockScratch& s) {
-    const int per = (nbins + kNT - 1) / kNT;
-    const int b0 = threadIdx.x * per;
-    ff Mf = ff{0.0f, 0.0f};
-    for (int i = 0; i < per; ++i) {
-        const int b = b0 + i;
-        if (b >= nbins) break;
-        const uint32_t cnt = hist[b];
-        if (cnt == 0) continue;
-        const float x = bf16_bits_to_float(okey16_to_bits((uint32_t)(key_top - b)));
-        const float w = weight_of(x, c, mc);
-        const float p = (float)cnt * w;
-        Mf = ff_add(Mf, ff{p, fmaf((float)cnt, w, -p)});  // exact product as a pair
-    }
-    ff totf;
-    const ff Sf = block_exclusive_scan_ff(Mf, s, &totf);
-    const double Mt = ff_to_double(Mf), St = ff_to_double(Sf), tot = ff_to_double(totf);
-    if (threadIdx.x == 0) s.bcast_i[1] = 0;
-    __syncthreads();
-    if (Mt > 0.0 && F0 + St < pZ && F0 + St + Mt >= pZ) {
-        double F = F0 + St;
-        int last = -1;
-        for (int i = 0; i < per; ++i) {
-            const int b = b0 + i;
-            if (b >= nbins) break;
-            const uint32_t cnt = hist[b];
-            if (cnt == 0) continue;
-            last = b;
-            const float x = bf16_bits_to_float(okey16_to_bits((uint32_t)(key_top - b)));
-            const double w = (double)weight_of(x, c, mc);
-            if (F + (double)cnt * w >= pZ) {
-                int nk = (int)ceil((pZ - F) / w);
-                nk = nk < 1 ? 1 : (nk > (int)cnt ? (int)cnt : nk);
-                s.bcast_f[0] = x;
-                s.bcast_i[2] = nk;
-                s.bcast_i[3] = (int)cnt;
-                s.bcast_d[0] = F + (double)nk * w;
-                s.bcast_i[1] = 1;
-                last = -2;
-                break;
-            }
-            F += (double)cnt * w;
-        }
-        if (last >= 0) {  // pZ at the chunk's very end after rounding: keep the last bucket whole
-            s.bcast_f[0] = bf16_bits_to_float(okey16_to_bits((uint32_t)(key_top - last)));
-            s.bcast_i[2] = (int)hist[last];
-            s.bcast_i[3] = (int)hist[last];
-            s.bcast_d[0] = F;
-            s.bcast_i[1] = 1;
-        }
-    }
-    __syncthreads();
-    Topp r;
-    r.ok = s.bcast_i[1] != 0;
-    r.tau = s.bcast_f[0];
-    r.n_keep = s.bcast_i[2];
-    r.c_tau = s.bcast_i[3];
-    r.mass = s.bcast_d[0];
-    if (F_end) *F_end = F0 + tot;
-    __syncthreads();
-    return r;
+// Smallest n in [1, cnt] with F + n * w >= pZ, for F < pZ <= F + cnt * w
+// (products formed exactly, differences in float-float).
+__device__ __forceinline__ int keep_count(ff F, ff pZ, float w, int cnt) {
+    const ff d = ff_sub(pZ, F);
+    int n = (int)ceilf(ff_to_float(d) / w);
+    n = n < 1 ? 1 : (n > cnt ? cnt : n);
+    if (n > 1 && ff_ge(ff_two_prod((float)(n - 1), w), d)) --n;
+    else if (n < cnt && ff_lt(ff_two_prod((float)n, w), d)) ++n;
+    return n;
 }
 
 // Lower bound on the nucleus boundary: a token of weight w <= (1 - top_p) *
-// Z / V cannot be kept (the tail from the crossing token on holds more than
-// (1 - top_p) * Z in at most V tokens, none heavier than it).  Returned as a
-// value a little below that bound.
-__device__ __forceinline__ float nucleus_lower_bound(float m, double Z, float top_p, int V, float c) {
-    const float wb = 0.5f * (1.0f - top_p) * (float)Z / (float)V;
+// Z / V cannot be kept (the tail from that token on holds at most V tokens,
+// none heavier, so it weighs at most (1 - top_p) * Z and everything before
+// it already reaches top_p * Z).  Returned as a value a little below that.
+__device__ __forceinline__ float nucleus_lower_bound(float m, ff Z, float top_p, int V, float c) {
+    const float wb = 0.5f * (1.0f - top_p) * ff_to_float(Z) / (float)V;
+    if (!(wb > 0.0f)) return -INFINITY;
     return m + log2f(wb) / c;
 }
 
-// Exact nucleus by count histograms of the 16-bit keys over successive
-// windows of kFullBins keys below the max, walked from the top.  Keys below
-// the weight bound are never counted.  Shared memory: kFullBins words.
-__device__ inline Topp row_topp_bf16_full(const __nv_bfloat16* __restrict__ row, int V, float c, float m, double Z,
-                                          float top_p, uint32_t* hist, BlockScratch& s, int key_floor = -1) {
-    const RowView<__nv_bfloat16> rv(row, V);
-    const int tid = threadIdx.x;
-    const float mc = scaled_max(m, c);
-    const int kmax = (int)value_key(m);
-    const double pZ = (double)top_p * Z;
-    // keys <= 0x7f are -inf and negative NaNs: zero weight, never the boundary
-    int oklo = (int)okey16(bf16_bits_round_down(nucleus_lower_bound(m, Z, top_p, V, c))) - 2;
-    if (oklo < 0x80) oklo = 0x80;
-    if (key_floor > oklo) oklo = key_floor;
-    double F0 = 0.0;
-    for (int hi_ok = kmax; hi_ok >= oklo;) {
-        int lo_ok = hi_ok - kFullBins + 1;
-        if (lo_ok < oklo) lo_ok = oklo;
-        if (lo_ok == 0x8000 && hi_ok > 0x8000) lo_ok = 0x8001;  // keep +0 and -0 in one window
-        const int nb = hi_ok - lo_ok + 1;
-        for (int i = tid; i < kFullBins / 4; i += kNT) reinterpret_cast<uint4*>(hist)[i] = make_uint4(0, 0, 0, 0);
-        __syncthreads();
-        const uint4* vp = rv.vec();
-        for (int u = tid; u < rv.units(); u += kNT) {
-            int i0, cnt;
-            rv.unit_range(u, i0, cnt);
-            uint32_t w[4];
-            if (u >= 1 && u <= rv.nvec) {
-                const uint4 v = __ldg(vp + (u - 1));
-                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
-            } else {
-                const unsigned short* p16 = reinterpret_cast<const unsigned short*>(row) + i0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t lo = (2 * j < cnt) ? p16[2 * j] : 0xff80u;
-                    const uint32_t hi = (2 * j + 1 < cnt) ? p16[2 * j + 1] : 0xff80u;
-                    w[j] = lo | (hi << 16);
-                }
+// Walk of consecutive keys from the top (position 0 holds key key_top,
+// position p key key_top - p) from mass F0 above key_top, looking for the
+// key where the running mass reaches pZ.  ASC = false: hist[p] is the
+// count at position p; ASC = true: hist[nbins - 1 - p].  A map may put a
+// "lump" at one position: the values too close to zero to count key by key,
+// given by their exact total mass; positions after it continue from
+// key_below.  Position masses are formed exactly per key (count * weight as
+// a pair) and summed in float-float; the crossing chunk is the lowest-index
+// one whose end reaches pZ, and its owner walks it.  WARP = true: warp 0
+// walks (the other warps only meet the barriers).
+// found: 0 the window ends first (*F_end: mass above its bottom); 1 found;
+// 2 the crossing lies inside the lump (F_lump: the mass above the lump).
+struct WalkMap {
+    int key_top;
+    int lump;       // position of the lump, or -1
+    int key_below;  // key at position lump + 1
+    ff lump_mass;
+};
+__device__ __forceinline__ WalkMap plain_map(int key_top) { return WalkMap{key_top, -1, 0, ff{0.0f, 0.0f}}; }
+struct WalkOut {
+    int found;
+    Topp r;
+    ff F_lump;
+};
+template <bool WARP, bool ASC = false>
+__device__ WalkOut walk_keys(const uint32_t* hist, int nbins, const WalkMap& map, float c, float mc, ff F0, ff pZ,
+                             ff* F_end, BlockScratch& s) {
+    auto count_at = [&](int p) -> uint32_t { return hist[ASC ? nbins - 1 - p : p]; };
+    auto key_at = [&](int p) -> int {
+        return (map.lump < 0 || p < map.lump) ? map.key_top - p : map.key_below - (p - map.lump - 1);
+    };
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int nparts = WARP ? 32 : kNT;
+    const int part = WARP ? lane : tid;
+    const bool active = !WARP || tid < 32;
+    const int per = (nbins + nparts - 1) / nparts;
+    const int b0 = part * per;
+    ff M = ff{0.0f, 0.0f};
+    if (active) {
+        for (int i = 0; i < per; ++i) {
+            const int b = b0 + i;
+            if (b >= nbins) break;
+            if (b == map.lump) {
+                M = ff_add(M, map.lump_mass);
+                continue;
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t b = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xffffu);
-                const int ok = (int)okey16(b);
-                if (ok >= lo_ok && ok <= hi_ok) atomicAdd(&hist[hi_ok - ok], 1u);
-            }
+            const uint32_t cnt = count_at(b);
+            if (cnt == 0) continue;
+            M = ff_add(M, ff_two_prod((float)cnt, weight_of(key_value(key_at(b)), c, mc)));
         }
-        __syncthreads();
-        // -0 and +0 are one value: fold the -0 count onto +0
-        if (tid == 0 && hi_ok >= 0x8000 && lo_ok <= 0x7fff) {
-            hist[hi_ok - 0x8000] += hist[hi_ok - 0x7fff];
-            hist[hi_ok - 0x7fff] = 0;
-        }
-        __syncthreads();
-        double F_end;
-        const Topp r = scan_key_bins(hist, nb, hi_ok, c, mc, F0, pZ, &F_end, s);
-        if (r.ok) return r;
-        F0 = F_end;
-        hi_ok = lo_ok - 1;
     }
-    Topp r;  // not reached above key_floor (or, without a floor, only by rounding)
-    r.ok = false;
-    r.tau = -INFINITY;
-    r.n_keep = 0;
-    r.c_tau = 0;
-    r.mass = F0 > 0.0 ? F0 : Z;
-    return r;
+    ff before = ff{0.0f, 0.0f}, tot = ff{0.0f, 0.0f};
+    if (WARP) {
+        if (active) {
+            const ff incl = warp_inclusive_scan_ff(M);
+            const ff up = ff_shfl_up(incl, 1);
+            before = lane == 0 ? ff{0.0f, 0.0f} : up;
+            tot = ff_shfl(incl, 31);
+        }
+    } else {
+        before = block_exclusive_scan_ff(M, s, &tot);
+    }
+    // lowest part whose end reaches pZ
+    int cand = 0x7fffffff;
+    if (active && M.hi > 0.0f && ff_ge(ff_add(ff_add(F0, before), M), pZ)) cand = part;
+    int first = 0x7fffffff;
+    if (WARP) {
+        if (active) {
+            const unsigned bal = __ballot_sync(0xffffffffu, cand != 0x7fffffff);
+            first = bal ? __ffs(bal) - 1 : 0x7fffffff;
+        }
+    } else {
+        first = block_min_i(cand, s);
+    }
+    if (first == 0x7fffffff && tid == 0) s.bcast_i[0] = 0;  // otherwise the crossing part writes it
+    if (active && part == first) {
+        ff F = ff_add(F0, before);
+        int last = -1;
+        ff F_last = F;  // mass above the last nonzero position
+        int res = 0;
+        for (int i = 0; i < per; ++i) {
+            const int b = b0 + i;
+            if (b >= nbins) break;
+            if (b == map.lump) {
+                if (!(map.lump_mass.hi > 0.0f)) continue;
+                const ff nxt = ff_add(F, map.lump_mass);
+                if (ff_ge(nxt, pZ)) {
+                    s.bcast_f[1] = F.hi;
+                    s.bcast_f[2] = F.lo;
+                    res = 2;
+                    break;
+                }
+                F_last = F;
+                F = nxt;
+                last = b;
+                continue;
+            }
+            const uint32_t cnt = count_at(b);
+            if (cnt == 0) continue;
+            const float w = weight_of(key_value(key_at(b)), c, mc);
+            const ff nxt = ff_add(F, ff_two_prod((float)cnt, w));
+            if (ff_ge(nxt, pZ)) {
+                const int nk = keep_count(F, pZ, w, (int)cnt);
+                const ff mass = ff_add(F, ff_two_prod((float)nk, w));
+                s.bcast_f[0] = key_value(key_at(b));
+                s.bcast_f[1] = mass.hi;
+                s.bcast_f[2] = mass.lo;
+                s.bcast_i[1] = nk;
+                s.bcast_i[2] = (int)cnt;
+                res = 1;
+                break;
+            }
+            F_last = F;
+            F = nxt;
+            last = b;
+        }
+        if (res == 0 && last >= 0) {  // the sequential sum fell short by rounding: take the last bucket
+            if (last == map.lump) {
+                s.bcast_f[1] = F_last.hi;
+                s.bcast_f[2] = F_last.lo;
+                res = 2;
+            } else {
+                s.bcast_f[0] = key_value(key_at(last));
+                s.bcast_f[1] = F.hi;
+                s.bcast_f[2] = F.lo;
+                s.bcast_i[1] = (int)count_at(last);
+                s.bcast_i[2] = (int)count_at(last);
+                res = 1;
+            }
+        }
+        s.bcast_i[0] = res;
+    }
+    if (WARP && tid < 32) {  // the total for F_end, from lane 0
+        if (lane == 0) { s.bcast_f[3] = tot.hi; s.bcast_f[4] = tot.lo; }
+    } else if (!WARP && tid == 0) {
+        s.bcast_f[3] = tot.hi;
+        s.bcast_f[4] = tot.lo;
+    }
+    __syncthreads();
+    WalkOut o;
+    o.found = s.bcast_i[0];
+    o.r.tau = s.bcast_f[0];
+    o.r.mass = ff{s.bcast_f[1], s.bcast_f[2]};
+    o.r.n_keep = s.bcast_i[1];
+    o.r.c_tau = s.bcast_i[2];
+    o.F_lump = o.r.mass;
+    if (F_end) *F_end = ff_add(F0, ff{s.bcast_f[3], s.bcast_f[4]});
+    __syncthreads();
+    return o;
 }
 
-// Exact nucleus guided by the pass-1 sample (bf16 rows).
-//  1. From the sample and the exact Z, estimate where the mass strictly
-//     below t reaches (1 - top_p) * Z: the tail is made of many light
-//     tokens, so a 1/32 sample estimates it well, and the few heavy tokens
-//     (which the sample may miss) sit far above it.  Widen by a
-//     sampling-error margin into a bracket [t_a, t_b] of bf16 values.
-//  2. Re-read the row (from L2): exact mass strictly above t_b, and exact
-//     counts of the keys inside the bracket.
-//  3. Walk the bracket from the top.  ok = false when the crossing is not
-//     inside it; the caller then runs the full method.
-// Before that, a peaked row takes a cheaper exact route: each thread's
-// maximum is a distinct element, so when the maxima at or above t already
-// weigh top_p * Z, the boundary lies above t; if few tokens are estimated
-// above that t, all of them are counted exactly (no mass pass needed).
-// smem: kTopSmemBytes holding the pass-1 sample and thread maxima.
-__device__ inline Topp row_topp_bf16_guided(const __nv_bfloat16* __restrict__ row, int V, float c, float m, double Z,
-                                            float top_p, uint8_t* smem, BlockScratch& s) {
-    const uint16_t* sample = reinterpret_cast<const uint16_t*>(smem);
-    uint32_t* band = reinterpret_cast<uint32_t*>(smem + kBandOffset);
-    uint32_t* wcount = reinterpret_cast<uint32_t*>(smem + kCoarseOffset);  // per-warp u16 pairs
-    int* tmcount = reinterpret_cast<int*>(smem + kTmCountOffset);         // thread-maximum counts
-    int* ccount = reinterpret_cast<int*>(smem + kBandOffset);             // merged sample counts
-    const float* tmax = reinterpret_cast<const float*>(smem + kTmaxOffset);
-    const int tid = threadIdx.x;
-    const float mc = scaled_max(m, c);
-    const double pZ = (double)top_p * Z;
-    const float tlo = nucleus_lower_bound(m, Z, top_p, V, c);
-    const float span = m - tlo;
-    Topp fail;
-    fail.ok = false;
-    if (!(span > 0.0f) || !(span < INFINITY)) return fail;
-
-    // 1. estimate from the sample (bin kCoarseBins collects values below tlo)
-    for (int i = tid; i < kNW * kCoarseWords; i += kNT) wcount[i] = 0u;
-    for (int i = tid; i <= kCoarseBins; i += kNT) tmcount[i] = 0;
-    __syncthreads();
-    const float inv_w = (float)kCoarseBins / span;
-    {
-        const float x = tmax[tid];
-        if (x >= tlo) {
-            int bin = (int)((m - x) * inv_w);
-            bin = bin < 0 ? 0 : (bin > kCoarseBins - 1 ? kCoarseBins - 1 : bin);
-            atomicAdd(&tmcount[bin], 1);
-        }
-    }
-    int nvalid = 0;
-    for (int i = tid; i < kSampleCap; i += kNT) {
-        const uint32_t b = sample[i];
-        if ((b & 0x7fffu) > 0x7f80u) continue;  // empty slot (NaN pattern)
-        const float x = bf16_bits_to_float(b);
-        ++nvalid;
-        int bin = kCoarseBins;
-        if (x >= tlo) {
-            bin = (int)((m - x) * inv_w);
-            bin = bin < 0 ? 0 : (bin > kCoarseBins - 1 ? kCoarseBins - 1 : bin);
-        }
-        atomicAdd(&wcount[(tid >> 5) * kCoarseWords + (bin >> 1)], 1u << ((bin & 1) * 16));
-    }
-    const int S = block_sum_i(nvalid, s);
-    // merge the per-warp counters (block_sum_i above ended with a barrier)
-    for (int i = tid; i <= kCoarseBins; i += kNT) {
-        int t = 0;
-        for (int w = 0; w < kNW; ++w) t += (int)((wcount[w * kCoarseWords + (i >> 1)] >> ((i & 1) * 16)) & 0xffffu);
-        ccount[i] = t;
-    }
-    __syncthreads();
-    // Warp 0 turns the bins into the decision: prefix sums in fixed point,
-    // crossings found by ballot.  Bottom-up positions q: q = 0 is the bin
-    // below tlo, q >= 1 is coarse bin j = kCoarseBins - q (rising values).
-    if (tid < 32) {
-        const int lane = tid;
-        // peaked route (top-down over bins j): thread maxima against top_p * Z
-        int floor_key = -1;
-        {
-            // each thread maximum in bin j weighs at least the weight of the
-            // bin's lower edge, so these masses never exceed the true ones
-            unsigned long long tm[8], cum = 0ull;
-            int cn[8], ccum = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int j = 8 * lane + i;
-                const float w_lo = weight_of(m - (float)(j + 1) / inv_w, c, mc);
-                tm[i] = (unsigned long long)tmcount[j] * (unsigned long long)(w_lo * kFixF);
-                cn[i] = ccount[j];
-                cum += tm[i];
-                ccum += cn[i];
-            }
-            unsigned long long pre = cum;
-            int cpre = ccum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xffffffffu, pre, o);
-                const int yc = __shfl_up_sync(0xffffffffu, cpre, o);
-                if (lane >= o) { pre += y; cpre += yc; }
-            }
-            pre -= cum;
-            cpre -= ccum;
-            const unsigned long long pZf = (unsigned long long)(pZ * kFix);
-            int hit = -1, nab = 0;
-            for (int i = 0; i < 8 && hit < 0; ++i) {
-                pre += tm[i];
-                cpre += cn[i];
-                if (pre >= pZf) { hit = 8 * lane + i; nab = cpre; }
-            }
-            const unsigned bal = __ballot_sync(0xffffffffu, hit >= 0);
-            if (bal) {
-                const int src = __ffs(bal) - 1;
-                const int jp = __shfl_sync(0xffffffffu, hit, src);
-                const int nabove_s = __shfl_sync(0xffffffffu, nab, src);
-                const double nabove = S > 0 ? (double)nabove_s * (double)V / (double)S : (double)V;
-                if (nabove <= (double)V / 64.0 || S < 512) {
-                    const float edge = m - (float)(jp + 1) / inv_w;
-                    floor_key = (int)value_key(bf16_bits_to_float(bf16_bits_round_down(edge < tlo ? tlo : edge))) - 1;
-                }
-            }
-        }
-        // sampled bracket (bottom-up over positions q)
-        int key_a = -1, key_b = -1;
-        if (floor_key < 0 && S >= 512) {
-            unsigned long long mm[9], cum = 0ull;
-            int cc[9], ccum = 0;
-#pragma unroll
-            for (int i = 0; i < 9; ++i) {
-                const int q = 9 * lane + i;
-                const int idx = (q == 0) ? kCoarseBins : kCoarseBins - q;
-                const float xc = (q == 0) ? tlo : m - ((float)idx + 0.5f) / inv_w;  // bin centre
-                cc[i] = (q <= kCoarseBins) ? ccount[idx] : 0;
-                mm[i] = (unsigned long long)cc[i] * (unsigned long long)(weight_of(xc, c, mc) * kFixF);
-                cum += mm[i];
-                ccum += cc[i];
-            }
-            unsigned long long pre = cum;
-            int cpre = ccum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(0xffffffffu, pre, o);
-                const int yc = __shfl_up_sync(0xffffffffu, cpre, o);
-                if (lane >= o) { pre += y; cpre += yc; }
-            }
-            pre -= cum;
-            cpre -= ccum;
-            const double T0 = (1.0 - (double)top_p) * Z * (double)S / (double)V;
-            // first position whose running mass reaches a threshold (9*32 if none)
-            auto first_ge = [&](unsigned long long thr, int* count_at) -> int {
-                unsigned long long r = pre;
-                int rc = cpre, hit = -1, hc = 0;
-                for (int i = 0; i < 9; ++i) {
-                    r += mm[i];
-                    rc += cc[i];
-                    if (hit < 0 && r >= thr && 9 * lane + i <= kCoarseBins) { hit = 9 * lane + i; hc = rc; }
-                }
-                const unsigned bal = __ballot_sync(0xffffffffu, hit >= 0);
-                if (!bal) return 9 * 32;
-                const int src = __ffs(bal) - 1;
-                if (count_at) *count_at = __shfl_sync(0xffffffffu, hc, src);
-                return __shfl_sync(0xffffffffu, hit, src);
-            };
-            int ncross = 0;
-            const int qx = first_ge((unsigned long long)(T0 * kFix), &ncross);
-            if (qx <= kCoarseBins && ncross > 0) {
-                const double eps = 4.0 / sqrt((double)ncross) + 0.03;
-                const int qa_next = first_ge((unsigned long long)fmax(0.0, T0 * (1.0 - eps) * kFix) + 1ull, nullptr);
-                const int qb = first_ge((unsigned long long)(T0 * (1.0 + eps) * kFix), nullptr);
-                if (qb <= kCoarseBins) {
-                    const int qa = qa_next - 1;  // last position still at or below T0 * (1 - eps)
-                    const int ja = (qa >= 1) ? kCoarseBins - qa : kCoarseBins;
-                    const int jb = kCoarseBins - (qb > 1 ? qb : 1);
-                    // widen by one bin on each side
-                    const float ta = (ja >= kCoarseBins) ? tlo : m - (float)(ja + 2) / inv_w;
-                    const float tb = m - (float)(jb - 1) / inv_w;
-                    const float ta_c = ta < tlo ? tlo : ta;
-                    const float tb_c = tb > m ? m : tb;
-                    key_a = (int)value_key(bf16_bits_to_float(bf16_bits_round_down(ta_c)));
-                    key_b = (int)value_key(bf16_bits_to_float(bf16_bits_round_down(tb_c)));
-                    if (key_a <= 0x8000 && key_b >= 0x8000) key_a = key_a < 0x7fff ? key_a : 0x7fff;  // include -0
-                    if (key_a < 0x80) key_a = 0x80;
-                    if (key_b - key_a + 1 > kBandBins || key_b < key_a) key_a = -1;
-                }
-            }
-        }
-        if (lane == 0) {
-            s.bcast_i[0] = key_a;
-            s.bcast_i[1] = key_b;
-            s.bcast_i[2] = floor_key;
-        }
-    }
-    __syncthreads();
-    const int floor_key = s.bcast_i[2];
-    if (floor_key >= 0) {
-        __syncthreads();
-        return row_topp_bf16_full(row, V, c, m, Z, top_p, reinterpret_cast<uint32_t*>(smem), s, floor_key);
-    }
-    const int key_a = s.bcast_i[0], key_b = s.bcast_i[1];
-    __syncthreads();
-    if (key_a < 0) return fail;
-    const int W = key_b - key_a + 1;
-    const float t_b = bf16_bits_to_float(okey16_to_bits((uint32_t)key_b));
-    const float t_a = bf16_bits_to_float(okey16_to_bits((uint32_t)key_a));
-
-    // 2. exact mass above t_b and exact counts inside [t_a, t_b]
-    const bool per_warp = W <= kBandBinsWarp;
-    const int nwords = per_warp ? kNW * W : W;
-    for (int i = tid; i < nwords; i += kNT) band[i] = 0u;
-    __syncthreads();
-    uint32_t* myband = per_warp ? band + (tid >> 5) * W : band;
+// Counts of the keys in [klo, khi] into hist[khi - key]; -0 is counted as
+// +0 when both are in the window.
+__device__ inline void count_key_window(const __nv_bfloat16* __restrict__ row, int V, int klo, int khi,
+                                        uint32_t* hist, BlockScratch& s) {
     const RowView<__nv_bfloat16> rv(row, V);
-    // Per 16-byte vector: the weights of elements above t_b (others get
-    // 2^-inf = 0) summed with packed FP32 pairs, and an 8-bit mask of the
-    // elements inside the bracket, whose keys are counted in one branch.
-    const float2 cc = make_float2(c, c), nmc = make_float2(-mc, -mc);
-    float fsum = 0.0f, fcomp = 0.0f;  // Kahan pair across batches
-    // Histogram index key_b - key(b): one add when the bracket lies on one
-    // side of zero (keys of one sign are affine in the bit pattern).
-    const int sgn = (key_a >= 0x8000) ? 0 : (key_b <= 0x7fff ? 1 : 2);
-    const uint32_t kpos = (uint32_t)(key_b - 0x8000), kneg = (uint32_t)(key_b - 0xffff);
-    auto count_key = [&](uint32_t b) {
-        if (sgn == 0) atomicAdd(&myband[kpos - b], 1u);
-        else if (sgn == 1) atomicAdd(&myband[kneg + b], 1u);
-        else {
-            const uint32_t idx = (uint32_t)(key_b - (int)okey16(b));
-            if (idx < (uint32_t)W) atomicAdd(&myband[idx], 1u);
-        }
+    const int tid = threadIdx.x;
+    const int nb = khi - klo + 1;
+    for (int i = tid; i < nb; i += kNT) hist[i] = 0u;
+    __syncthreads();
+    auto take = [&](uint32_t b) {
+        const uint32_t idx = (uint32_t)(khi - (int)okey16(b));
+        if (idx < (uint32_t)nb) atomicAdd(&hist[idx], 1u);
     };
-    auto vec_mass = [&](const uint4& v) -> float {
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-        float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float2 x = make_float2(bf16_lo(w4[j]), bf16_hi(w4[j]));
-            float2 t = __ffma2_rn(x, cc, nmc);
-            const bool ax = x.x > t_b, ay = x.y > t_b;
-            t.x = ax ? t.x : -INFINITY;
-            t.y = ay ? t.y : -INFINITY;
-            acc = __fadd2_rn(acc, make_float2(ex2(t.x), ex2(t.y)));
-            if (!ax && x.x >= t_a) count_key(w4[j] & 0xffffu);
-            if (!ay && x.y >= t_a) count_key(w4[j] >> 16);
-        }
-        return acc.x + acc.y;
-    };
-    auto take_scalar = [&](uint32_t b) {
-        const float x = bf16_bits_to_float(b);
-        fsum += (x > t_b) ? weight_of(x, c, mc) : 0.0f;
-        if (x >= t_a && x <= t_b) count_key(b);
-    };
-    if (tid < rv.head) take_scalar(*reinterpret_cast<const unsigned short*>(row + tid));
+    if (tid < rv.head) take(*reinterpret_cast<const unsigned short*>(row + tid));
     const uint4* vp = rv.vec();
-    constexpr int kU2 = 4;  // the re-read comes from L2: fewer vectors in flight suffice
+    constexpr int kU2 = 4;
     for (int base = tid; base < rv.nvec; base += kU2 * kNT) {
         uint4 v[kU2];
 #pragma unroll
         for (int u = 0; u < kU2; ++u) {
             const int vi = base + u * kNT;
+            v[u] = (vi < rv.nvec) ? __ldg(vp + vi) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+        }
+#pragma unroll
+        for (int u = 0; u < kU2; ++u) {
+            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                take(w4[j] & 0xffffu);
+                take(w4[j] >> 16);
+            }
+        }
+    }
+    if (tid < rv.tail) take(*reinterpret_cast<const unsigned short*>(row + rv.head + rv.nvec * 8 + tid));
+    __syncthreads();
+    if (tid == 0 && khi >= 0x8000 && klo <= 0x7fff) {
+        hist[khi - 0x8000] += hist[khi - 0x7fff];
+        hist[khi - 0x7fff] = 0u;
+    }
+    __syncthreads();
+}
+
+// Exact nucleus by counting key windows from key_top down to key_floor,
+// starting at mass F0 above key_top.  Each window is one pass over the row
+// (from L2) and one walk.
+__device__ inline Topp topp_windows(const __nv_bfloat16* __restrict__ row, int V, float c, float mc, ff Z, ff pZ,
+                                    int key_top, int key_floor, ff F0, uint32_t* hist, BlockScratch& s) {
+    if (key_floor == 0x8000) key_floor = 0x7fff;  // -0 belongs with +0
+    for (int hi = key_top; hi >= key_floor;) {
+        int lo = hi - kFullBins + 1;
+        if (lo < key_floor) lo = key_floor;
+        if (lo == 0x8000 && hi > 0x8000) lo = 0x8001;  // keep +0 and -0 in one window
+        count_key_window(row, V, lo, hi, hist, s);
+        ff F_end;
+        const WalkOut o = walk_keys<false>(hist, hi - lo + 1, plain_map(hi), c, mc, F0, pZ, &F_end, s);
+        if (o.found == 1) return o.r;
+        F0 = F_end;
+        hi = lo - 1;
+    }
+    Topp r;  // reached only by rounding: keep every token
+    r.tau = -INFINITY;
+    r.n_keep = 0;
+    r.c_tau = 0;
+    r.mass = Z;
+    return r;
+}
+
+__device__ __forceinline__ float warp_sum_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Second pass of the bracketed route, one read of the row (from L2): the
+// exact mass of the elements above t_b (returned as this thread's part) and
+// the exact counts of the keys in [t_a, t_b].  SGN 0: the bracket lies above
+// +0, counts in hist[key - key_a]; 1: below -0, hist[key_b - key].  A count
+// is addressed by one add to the element's float bit pattern shifted right
+// by 14 (4 * its bf16 bits).
+template <int SGN>
+__device__ ff band_pass(const __nv_bfloat16* __restrict__ row, int V, float c, float mc, int key_a, int key_b,
+                        uint32_t* hist) {
+    const RowView<__nv_bfloat16> rv(row, V);
+    const int tid = threadIdx.x;
+    const float t_a = key_value(key_a), t_b = key_value(key_b);
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(hist);
+    const uint32_t k0 = base - 4u * (uint32_t)(key_a - 0x8000);  // SGN 0: k0 + 4 * bits
+    const uint32_t k1 = base - 4u * (uint32_t)(0xffff - key_b);  // SGN 1: k1 + 4 * bits
+    const uint32_t kb = (SGN == 0) ? k0 : k1;
+    // One element, branch-free: returns x's exponent argument when x is above
+    // t_b (-inf otherwise) and counts x when it lies inside [t_a, t_b]; xb is
+    // x's float bit pattern (bf16 bits << 16).
+    auto element = [&](float x, uint32_t xb, float t) -> float {
+        float r;
+        asm volatile(
+            "{\n\t.reg .pred pa, pb;\n\t"
+            "setp.gt.f32 pa, %1, %3;\n\t"
+            "selp.f32 %0, %2, 0fFF800000, pa;\n\t"
+            "setp.ge.and.f32 pb, %1, %4, !pa;\n\t"
+            "@pb red.shared.add.u32 [%5], 1;\n\t}"
+            : "=f"(r)
+            : "f"(x), "f"(t), "f"(t_b), "f"(t_a), "r"(kb + (xb >> 14))
+            : "memory");
+        return r;
+    };
+    const float2 cc = make_float2(c, c), nmc = make_float2(-mc, -mc);
+    float fsum = 0.0f, fcomp = 0.0f;  // Kahan pair across batches
+    auto vec_mass = [&](const uint4& v) -> float {
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t xl = w4[j] << 16, xh = w4[j] & 0xffff0000u;
+            const float2 x = make_float2(__uint_as_float(xl), __uint_as_float(xh));
+            float2 t = __ffma2_rn(x, cc, nmc);
+            t.x = element(x.x, xl, t.x);
+            t.y = element(x.y, xh, t.y);
+            acc = __fadd2_rn(acc, make_float2(ex2(t.x), ex2(t.y)));
+        }
+        return acc.x + acc.y;
+    };
+    auto take_scalar = [&](uint32_t b) {
+        const uint32_t xb = b << 16;
+        const float x = __uint_as_float(xb);
+        fsum += ex2(element(x, xb, fmaf(x, c, -mc)));
+    };
+    if (tid < rv.head) take_scalar(*reinterpret_cast<const unsigned short*>(row + tid));
+    const uint4* vp = rv.vec();
+    constexpr int kU2 = 4;  // the re-read comes from L2: fewer vectors in flight suffice
+    for (int base_v = tid; base_v < rv.nvec; base_v += kU2 * kNT) {
+        uint4 v[kU2];
+#pragma unroll
+        for (int u = 0; u < kU2; ++u) {
+            const int vi = base_v + u * kNT;
             v[u] = (vi < rv.nvec) ? __ldg(vp + vi) : neg_inf_vec<__nv_bfloat16>();
         }
         float bsum = 0.0f;
@@ -764,38 +760,332 @@ __device__ inline Topp row_topp_bf16_guided(const __nv_bfloat16* __restrict__ ro
         fsum = t;
     }
     if (tid < rv.tail) take_scalar(*reinterpret_cast<const unsigned short*>(row + rv.head + rv.nvec * 8 + tid));
-    const double F_above = ff_to_double(block_sum_ff(ff_add(ff{fsum, 0.0f}, ff{-fcomp, 0.0f}), s));
-    if (per_warp) {  // fold the warps' histograms into the first one
-        for (int i = tid; i < W; i += kNT) {
-            uint32_t t = 0u;
-            for (int w = 0; w < kNW; ++w) t += band[w * W + i];
-            band[i] = t;
-        }
-        __syncthreads();
-    }
-    if (tid == 0 && key_b >= 0x8000 && key_a <= 0x7fff) {
-        band[key_b - 0x8000] += band[key_b - 0x7fff];
-        band[key_b - 0x7fff] = 0;
-    }
-    __syncthreads();
-    if (F_above >= pZ) return fail;  // the boundary lies above the bracket
-
-    // 3. walk the bracket
-    return scan_key_bins(band, W, key_b, c, mc, F_above, pZ, nullptr, s);
+    return ff_add(ff{fsum, 0.0f}, ff{-fcomp, 0.0f});
 }
 
-// Exact top-p nucleus by bisection over 32-bit ordered keys (any element
-// type): the largest key K with mass(key >= K) >= top_p * Z.  One pass per
-// step, deterministic sums.
+// Key layout of a bracket that spans zero.  bf16 keys crowd near zero (every
+// binade down to the denormals), so values with |x| < 2^-10 form one lump,
+// measured by its exact mass; the keys above and below it are counted key by
+// key: positions [0, Wp) hold keys key_b, key_b - 1, ..., position Wp the
+// lump, positions after it keys kn_top, kn_top - 1, ... down to key_a.
+constexpr int kLumpPosKey = 0xBA80;  // key of +2^-10: smallest positive key counted one by one
+constexpr int kLumpNegKey = 0x457F;  // key of -2^-10: largest negative key counted one by one
+struct MixedLayout {
+    int key_a, key_b, Wp, Wn, kn_top;
+    __device__ MixedLayout(int ka, int kb) : key_a(ka), key_b(kb) {
+        Wp = (kb >= kLumpPosKey) ? kb - (ka > kLumpPosKey ? ka : kLumpPosKey) + 1 : 0;
+        kn_top = kb < kLumpNegKey ? kb : kLumpNegKey;
+        Wn = (ka <= kLumpNegKey) ? kn_top - ka + 1 : 0;
+    }
+    __device__ int bins() const { return Wp + 1 + Wn; }
+};
+
+// Second pass for a bracket spanning zero (layout above): exact mass above
+// t_b, exact mass of the lump, exact counts of the other keys inside.
+__device__ inline void band_pass_mixed(const __nv_bfloat16* __restrict__ row, int V, float c, float mc,
+                                       const MixedLayout& L, uint32_t* hist, ff& above, ff& lump) {
+    const RowView<__nv_bfloat16> rv(row, V);
+    const int tid = threadIdx.x;
+    const float t_a = key_value(L.key_a), t_b = key_value(L.key_b);
+    const float s0 = 0.0009765625f;  // 2^-10
+    auto take = [&](uint32_t b, float x, float w, float& fa, float& fl) {
+        if (x > t_b) {
+            fa += w;
+        } else if (x >= t_a) {
+            const int k = (int)okey16(b);
+            int idx;
+            if (k >= kLumpPosKey) idx = L.key_b - k;
+            else if (k > kLumpNegKey) idx = L.Wp, fl += w;
+            else idx = L.Wp + 1 + (L.kn_top - k);
+            atomicAdd(&hist[idx], 1u);
+        }
+    };
+    float fa = 0.0f, fl = 0.0f, ca = 0.0f;
+    auto weight_if = [&](float x) { return (x > t_b || fabsf(x) < s0) ? weight_of(x, c, mc) : 0.0f; };
+    if (tid < rv.head) {
+        const uint32_t b = *reinterpret_cast<const unsigned short*>(row + tid);
+        const float x = bf16_bits_to_float(b);
+        take(b, x, weight_if(x), fa, fl);
+    }
+    const uint4* vp = rv.vec();
+    for (int vi = tid; vi < rv.nvec; vi += kNT) {
+        const uint4 v = __ldg(vp + vi);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        float ba = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = w4[j] & 0xffffu, hi = w4[j] >> 16;
+            const float xl = bf16_bits_to_float(lo), xh = bf16_bits_to_float(hi);
+            take(lo, xl, weight_if(xl), ba, fl);
+            take(hi, xh, weight_if(xh), ba, fl);
+        }
+        const float y = ba - ca;  // Kahan across vectors
+        const float t = fa + y;
+        ca = (t - fa) - y;
+        fa = t;
+    }
+    if (tid < rv.tail) {
+        const uint32_t b = *reinterpret_cast<const unsigned short*>(row + rv.head + rv.nvec * 8 + tid);
+        const float x = bf16_bits_to_float(b);
+        take(b, x, weight_if(x), fa, fl);
+    }
+    above = ff_add(ff{fa, 0.0f}, ff{-ca, 0.0f});
+    lump = ff{fl, 0.0f};
+}
+
+// Exact nucleus of a bf16 row, guided by the pass-1 sample.
+//  1. Estimate (warp 0, from value-binned counts of the 1/32 sample and of
+//     the threads' maxima):
+//     - peaked rows: the thread maxima are distinct elements, so when those
+//       at or above some t already weigh top_p * Z (counted at lower-bound
+//       weights), the boundary provably lies at or above t; if few elements
+//       are estimated above t, they are all counted exactly (one pass, no
+//       weights needed);
+//     - otherwise the tail below the boundary is made of many light tokens
+//       and the sample estimates its mass with a computable standard error:
+//       the bracket [t_a, t_b] is where the estimated tail mass crosses
+//       (1 - top_p) * Z widened by four standard errors and one bin.
+//  2. One pass from L2: exact mass above t_b, exact key counts inside.
+//  3. Walk the bracket.  When the boundary is outside it, the exact counted
+//     windows take over from the side it lies on.
+// smem: kTopSmemBytes holding the pass-1 sample and thread maxima.
+__device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int V, float c, float m, ff Z,
+                                     float top_p, uint8_t* smem, BlockScratch& s) {
+    const uint16_t* sample = reinterpret_cast<const uint16_t*>(smem);
+    uint32_t* scount = reinterpret_cast<uint32_t*>(smem + kSCountOffset);
+    uint32_t* tcount = reinterpret_cast<uint32_t*>(smem + kTCountOffset);
+    const float* tmax = reinterpret_cast<const float*>(smem + kTmaxOffset);
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float mc = scaled_max(m, c);
+    const ff pZ = ff_mul_f(Z, top_p);
+    const float tlo = nucleus_lower_bound(m, Z, top_p, V, c);
+    const int kmax = (int)value_key(m);
+    int key_lo = (tlo > -INFINITY) ? (int)value_key(bf16_bits_to_float(bf16_bits_round_down(tlo))) - 2 : 0x80;
+    if (key_lo < 0x80) key_lo = 0x80;  // keys below are -inf and negative NaNs: zero weight
+    if (key_lo > kmax) key_lo = kmax;
+    const float span = m - tlo;
+    int route = 0, key_a = key_lo, key_b = kmax;  // route 0: counted windows from the top
+    if (span > 0.0f && span < INFINITY) {
+        const float inv_w = (float)kEstBins / span;
+        const float cdl = span / (float)kEstBins * c;  // log2 weight step of one bin
+        for (int i = tid; i < kEstBins / 4; i += kNT) {
+            reinterpret_cast<uint4*>(scount)[i] = make_uint4(0u, 0u, 0u, 0u);
+            reinterpret_cast<uint4*>(tcount)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        __syncthreads();
+        auto bin_of = [&](float x) {
+            const int j = (int)((m - x) * inv_w);
+            return j < 0 ? 0 : (j > kEstBins - 1 ? kEstBins - 1 : j);
+        };
+        {
+            const float x = tmax[tid];
+            if (x >= tlo) atomicAdd(&tcount[bin_of(x)], 1u);
+        }
+        int nv = 0;
+        float gb = 0.0f, vb = 0.0f;  // sampled mass (and squares) below tlo
+        for (int i = tid; i < kSampleCap; i += kNT) {
+            const uint32_t b = sample[i];
+            if ((b & 0x7fffu) > 0x7f80u) continue;  // empty slot
+            const float x = bf16_bits_to_float(b);
+            ++nv;
+            if (x >= tlo) {
+                atomicAdd(&scount[bin_of(x)], 1u);
+            } else {
+                const float w = weight_of(x, c, mc);
+                gb += w;
+                vb += w * w;
+            }
+        }
+        nv = warp_sum_i(nv);
+        gb = warp_sum_f(gb);
+        vb = warp_sum_f(vb);
+        if (lane == 0) {
+            s.pi[warp] = nv;
+            s.pf[warp] = gb;
+            s.pf2[warp] = vb;
+        }
+        __syncthreads();  // also publishes the bins
+        int S = 0;
+        float Gb = 0.0f, Vb = 0.0f;
+        for (int w = 0; w < kNW; ++w) {  // same order in every thread: identical values
+            S += s.pi[w];
+            Gb += s.pf[w];
+            Vb += s.pf2[w];
+        }
+        // this thread's bins j = kBinsPerThread * tid + i, j ascending from the max:
+        // thread maxima at lower-bound weights (tm), sample mass (sm), its squares (sv), counts (sn)
+        const int jt = kBinsPerThread * tid;
+        auto bin_vals = [&](int i, float& tmv, float& smv, float& svv, float& snv) {
+            const int j = jt + i;
+            const float jf = (float)j;
+            const uint32_t tc = tcount[j], sc = scount[j];
+            const float wc = ex2(-(jf + 0.5f) * cdl);
+            tmv = tc ? (float)tc * ex2(-(jf + 2.0f) * cdl) : 0.0f;
+            smv = (float)sc * wc;
+            svv = smv * wc;
+            snv = (float)sc;
+        };
+        float4 own = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int i = 0; i < kBinsPerThread; ++i) {
+            float a1, a2, a3, a4;
+            bin_vals(i, a1, a2, a3, a4);
+            own.x += a1; own.y += a2; own.z += a3; own.w += a4;
+        }
+        // prefixes over bins in j order (four quantities), warp by warp
+        float4 inc = own;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float a = __shfl_up_sync(0xffffffffu, inc.x, o), b = __shfl_up_sync(0xffffffffu, inc.y, o);
+            const float d = __shfl_up_sync(0xffffffffu, inc.z, o), e = __shfl_up_sync(0xffffffffu, inc.w, o);
+            if (lane >= o) { inc.x += a; inc.y += b; inc.z += d; inc.w += e; }
+        }
+        float4* wtot = reinterpret_cast<float4*>(smem + kWTotOffset);
+        if (lane == 31) wtot[warp] = inc;
+        __syncthreads();
+        float4 base = make_float4(0.0f, 0.0f, 0.0f, 0.0f), all = base;
+        for (int w = 0; w < kNW; ++w) {
+            const float4 t = wtot[w];
+            if (w < warp) { base.x += t.x; base.y += t.y; base.z += t.z; base.w += t.w; }
+            all.x += t.x; all.y += t.y; all.z += t.z; all.w += t.w;
+        }
+        // exclusive prefixes at this thread's first bin
+        const float pt0 = base.x + inc.x - own.x, pm0 = base.y + inc.y - own.y;
+        const float pv0 = base.z + inc.z - own.z, pn0 = base.w + inc.w - own.w;
+        // tail of the sample at bin j (values up to bin j's upper edge): G(j) = Gb + all.y - prefix_m(j)
+        const float thr_pk = pZ.hi * (1.0f + 1.0f / 4096.0f);
+        const float lower = 1.0f - 1.0f / 4096.0f;  // covers the rounding of the weights and sums
+        const float T0 = (1.0f - top_p) * ff_to_float(Z) * (float)S / (float)V;
+        int jp = 0x7fffffff, j0 = -1;
+        {
+            float rt = pt0, rm = pm0;
+            for (int i = 0; i < kBinsPerThread; ++i) {
+                float tmv, smv, svv, snv;
+                bin_vals(i, tmv, smv, svv, snv);
+                const int j = jt + i;
+                rt += tmv;
+                if (jp == 0x7fffffff && rt * lower >= thr_pk) jp = j;
+                if (Gb + (all.y - rm) >= T0) j0 = j;
+                rm += smv;
+            }
+            if (tid == 0 && Gb >= T0) j0 = max(j0, kEstBins);  // the position below tlo
+        }
+        int r1 = warp_min_i(jp), r2 = -warp_min_i(-j0);
+        if (lane == 0) { s.pi[warp] = r1; s.pi2[warp] = r2; }
+        __syncthreads();
+        int Jp = 0x7fffffff, J0 = -1;
+        for (int w = 0; w < kNW; ++w) { Jp = min(Jp, s.pi[w]); J0 = max(J0, s.pi2[w]); }
+        // the owners of bins Jp + 2 and J0 publish the sample count and the squares there
+        {
+            float rn = pn0, rv = pv0;
+            for (int i = 0; i < kBinsPerThread; ++i) {
+                float tmv, smv, svv, snv;
+                bin_vals(i, tmv, smv, svv, snv);
+                const int j = jt + i;
+                rn += snv;
+                if (Jp != 0x7fffffff && j == min(Jp + 2, kEstBins - 1)) s.bcast_f[5] = rn;
+                if (j == J0) s.bcast_f[6] = Vb + (all.z - rv);
+                rv += svv;
+            }
+            if (tid == 0 && J0 == kEstBins) s.bcast_f[6] = Vb;
+        }
+        __syncthreads();
+        const float ns = s.bcast_f[5], v0 = s.bcast_f[6];
+        if (Jp != 0x7fffffff && (S < 256 || 16.0f * ns <= (float)S)) {
+            route = 1;
+            const float t_f = m - (float)(Jp + 2) / inv_w;
+            key_a = (int)value_key(bf16_bits_to_float(bf16_bits_round_down(t_f < tlo ? tlo : t_f)));
+            if (key_a < key_lo) key_a = key_lo;
+        } else if (S >= 256 && J0 >= 0 && T0 > 0.0f) {
+            float eps = 4.0f * sqrtf(v0) / T0 + 2.0f * cdl + 0.002f;
+            eps = eps > 0.9f ? 0.9f : eps;
+            const float Ta = T0 * (1.0f - eps), Tb = T0 * (1.0f + eps);
+            int ja = -1, jb = -1;
+            float rm = pm0;
+            for (int i = 0; i < kBinsPerThread; ++i) {
+                float tmv, smv, svv, snv;
+                bin_vals(i, tmv, smv, svv, snv);
+                const int j = jt + i;
+                const float G = Gb + (all.y - rm);
+                if (G >= Ta) ja = j;
+                if (G >= Tb) jb = j;
+                rm += smv;
+            }
+            if (tid == 0 && Gb >= Ta) ja = max(ja, kEstBins);
+            if (tid == 0 && Gb >= Tb) jb = max(jb, kEstBins);
+            r1 = -warp_min_i(-ja);
+            r2 = -warp_min_i(-jb);
+            __syncthreads();  // everyone has read the previous partials
+            if (lane == 0) { s.pi[warp] = r1; s.pi2[warp] = r2; }
+            __syncthreads();
+            int JA = -1, JB = -1;
+            for (int w = 0; w < kNW; ++w) { JA = max(JA, s.pi[w]); JB = max(JB, s.pi2[w]); }
+            // one bin of slack on each side
+            float ta = (JA >= kEstBins - 1) ? tlo : m - (float)(JA + 2) / inv_w;
+            float tb = m - (float)(JB - 1) / inv_w;
+            ta = ta < tlo ? tlo : ta;
+            tb = tb > m ? m : tb;
+            int ka = (int)value_key(bf16_bits_to_float(bf16_bits_round_down(ta)));
+            int kb = (int)value_key(bf16_bits_to_float(bf16_bits_round_down(tb)));
+            if (ka < key_lo) ka = key_lo;
+            if (kb > kmax) kb = kmax;
+            const bool spans = ka <= 0x8000 && kb >= 0x8000;
+            const int nb = spans ? MixedLayout(ka, kb).bins() : kb - ka + 1;
+            if (kb >= ka && nb <= kFullBins) {
+                route = 2;
+                key_a = ka;
+                key_b = kb;
+            }
+        }
+        __syncthreads();  // the estimate's shared memory becomes the histogram
+    }
+    if (route == 1) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_a, ff{0.0f, 0.0f}, hist, s);
+    if (route == 0) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_lo, ff{0.0f, 0.0f}, hist, s);
+
+    const bool spans = key_a <= 0x8000 && key_b >= 0x8000;
+    const MixedLayout L(key_a, key_b);
+    const int W = spans ? L.bins() : key_b - key_a + 1;
+    for (int i = tid; i < W; i += kNT) hist[i] = 0u;
+    __syncthreads();
+    ff part, lpart = ff{0.0f, 0.0f};
+    if (key_a > 0x8000) part = band_pass<0>(row, V, c, mc, key_a, key_b, hist);
+    else if (!spans) part = band_pass<1>(row, V, c, mc, key_a, key_b, hist);
+    else band_pass_mixed(row, V, c, mc, L, hist, part, lpart);
+    const ff F_above = block_sum_ff(part, s);  // its barriers also publish the counts
+    const ff lump = spans ? block_sum_ff(lpart, s) : ff{0.0f, 0.0f};
+    if (ff_ge(F_above, pZ))  // the boundary lies above the bracket
+        return topp_windows(row, V, c, mc, Z, pZ, kmax, key_b + 1, ff{0.0f, 0.0f}, hist, s);
+    ff F_end;
+    WalkOut o;
+    if (key_a > 0x8000) {
+        o = (W <= 2048) ? walk_keys<true, true>(hist, W, plain_map(key_b), c, mc, F_above, pZ, &F_end, s)
+                        : walk_keys<false, true>(hist, W, plain_map(key_b), c, mc, F_above, pZ, &F_end, s);
+    } else {
+        const WalkMap map = spans ? WalkMap{key_b, L.Wp, L.kn_top, lump} : plain_map(key_b);
+        o = (W <= 2048) ? walk_keys<true, false>(hist, W, map, c, mc, F_above, pZ, &F_end, s)
+                        : walk_keys<false, false>(hist, W, map, c, mc, F_above, pZ, &F_end, s);
+    }
+    if (o.found == 1) return o.r;
+    if (o.found == 2) {  // inside the lump: count its keys exactly, from the mass above it
+        const int top = key_b < kLumpPosKey - 1 ? key_b : kLumpPosKey - 1;
+        return topp_windows(row, V, c, mc, Z, pZ, top, key_lo, o.F_lump, hist, s);
+    }
+    // below the bracket: continue downwards from the exact mass above it
+    return topp_windows(row, V, c, mc, Z, pZ, key_a - 1, key_lo, F_end, hist, s);
+}
+
+// Exact nucleus by bisection over 32-bit ordered keys (any element type):
+// the largest key K with mass(key >= K) >= top_p * Z.  One pass per step,
+// float-float sums in a fixed order.
 template <typename T>
-__device__ Topp row_topp_bisect(const T* __restrict__ row, int V, float c, float m, double Z, float top_p,
+__device__ Topp row_topp_bisect(const T* __restrict__ row, int V, float c, float m, ff Z, float top_p,
                                 BlockScratch& s) {
     constexpr int VEC = ElemT<T>::VEC;
     const RowView<T> rv(row, V);
     const float mc = scaled_max(m, c);
-    const double pZ = (double)top_p * Z;
-    auto mass_ge = [&](uint32_t K, int* cnt_out) -> double {
-        double acc = 0.0;
+    const ff pZ = ff_mul_f(Z, top_p);
+    auto mass_ge = [&](uint32_t K, int* cnt_out) -> ff {
+        ff acc = ff{0.0f, 0.0f};
         int cnt = 0;
         for (int u = threadIdx.x; u < rv.units(); u += kNT) {
             float f[VEC];
@@ -803,37 +1093,35 @@ __device__ Topp row_topp_bisect(const T* __restrict__ row, int V, float c, float
             rv.load_unit(u, f, i0, n);
 #pragma unroll
             for (int j = 0; j < VEC; ++j) {
-                if (j < n && f[j] == f[j] && okey32(f[j]) >= K) {
-                    acc += (double)weight_of(f[j], c, mc);
+                if (j < n && okey32(f[j]) >= K) {
+                    acc = ff_add_f(acc, weight_of(f[j], c, mc));
                     ++cnt;
                 }
             }
         }
-        *cnt_out = block_sum_i(cnt, s);
-        return block_sum_d(acc, s);
+        if (cnt_out) *cnt_out = block_sum_i(cnt, s);
+        return block_sum_ff(acc, s);
     };
-    const uint32_t kmax = okey32(m);
-    uint64_t lo = 0, hi = (uint64_t)kmax + 1;  // mass(>= lo) >= pZ > mass(>= hi)
-    double F_hi = 0.0;
-    int c_hi = 0;
-    while (hi - lo > 1) {
-        const uint64_t mid = lo + (hi - lo) / 2;
+    // invariant: mass(>= lo) >= pZ, mass(>= hi) < pZ (hi = one above the max key)
+    uint32_t lo = 0x00800000u, hi = okey32(m) + 1u;  // keys below 0x00800000 are -inf and NaNs
+    ff F_hi = ff{0.0f, 0.0f};
+    while (hi - lo > 1u) {
+        const uint32_t mid = lo + (hi - lo) / 2u;
         int cm;
-        const double Fm = mass_ge((uint32_t)mid, &cm);
-        if (Fm >= pZ) lo = mid;
-        else { hi = mid; F_hi = Fm; c_hi = cm; }
+        const ff Fm = mass_ge(mid, &cm);
+        if (ff_ge(Fm, pZ)) lo = mid;
+        else { hi = mid; F_hi = Fm; }
     }
-    int c_lo;
-    mass_ge((uint32_t)lo, &c_lo);
     Topp r;
-    r.ok = true;
-    r.tau = okey32_to_float((uint32_t)lo);
+    r.tau = okey32_to_float(lo);
+    int c_lo;
+    mass_ge(lo, &c_lo);
+    int c_hi;
+    mass_ge(hi, &c_hi);
     r.c_tau = c_lo - c_hi;
-    const double w = (double)weight_of(r.tau, c, mc);
-    int nk = (int)ceil((pZ - F_hi) / w);
-    nk = nk < 1 ? 1 : (nk > r.c_tau ? r.c_tau : nk);
-    r.n_keep = nk;
-    r.mass = F_hi + (double)nk * w;
+    const float w = weight_of(r.tau, c, mc);
+    r.n_keep = (r.c_tau > 0) ? keep_count(F_hi, pZ, w, r.c_tau) : 0;
+    r.mass = ff_add(F_hi, ff_two_prod((float)r.n_keep, w));
     return r;
 }
 
@@ -842,7 +1130,7 @@ __device__ Topp row_topp_bisect(const T* __restrict__ row, int V, float c, float
 // smem: kTopSmemBytes of shared memory (MODE 2 with bf16 only).
 template <typename T, int MODE>
 __device__ RowStat row_stats(const T* __restrict__ row, int V, float c, float top_p, int tok, uint8_t* smem,
-                             BlockScratch& s) {
+                             BlockScratch& s, SampleScratch& ss) {
     constexpr bool kBand = (MODE == 2 && sizeof(T) == 2);
     const Pass1 p1 = row_pass1<T, (MODE > 0)>(row, V, c, s, kBand ? reinterpret_cast<uint16_t*>(smem) : nullptr,
                                               kBand ? reinterpret_cast<float*>(smem + kTmaxOffset) : nullptr);
@@ -854,12 +1142,9 @@ __device__ RowStat row_stats(const T* __restrict__ row, int V, float c, float to
     st.c_tau = 0;
     st.flags = 0;
     st.inv_zn = 0.0f;
-    if (threadIdx.x == 0) s.bcast_f[1] = (tok >= 0 && tok < V) ? ElemT<T>::load(row + tok) : __int_as_float(0x7fffffff);
-    __syncthreads();
-    st.x_tok = s.bcast_f[1];
-    __syncthreads();
+    st.x_tok = (tok >= 0 && tok < V) ? ElemT<T>::load(row + tok) : __int_as_float(0x7fffffff);
     bool valid = !p1.bad && p1.m > -INFINITY && p1.m < INFINITY;
-    if (MODE > 0) valid = valid && (p1.z > 0.0) && (p1.z < 1e300);
+    if (MODE > 0) valid = valid && (p1.z.hi > 0.0f) && (p1.z.hi < INFINITY);
     if (!valid) {
         st.flags = kRowInvalid;
         return st;
@@ -868,16 +1153,12 @@ __device__ RowStat row_stats(const T* __restrict__ row, int V, float c, float to
         st.flags = kRowTokMember;
         return st;
     }
-    double mass = p1.z;
+    ff mass = p1.z;
     bool member = true;
     if (MODE == 2) {
         Topp tp;
-        if constexpr (sizeof(T) == 2) {
-            tp = row_topp_bf16_guided(row, V, c, p1.m, p1.z, top_p, smem, s);
-            if (!tp.ok) tp = row_topp_bf16_full(row, V, c, p1.m, p1.z, top_p, reinterpret_cast<uint32_t*>(smem), s);
-        } else {
-            tp = row_topp_bisect<T>(row, V, c, p1.m, p1.z, top_p, s);
-        }
+        if constexpr (sizeof(T) == 2) tp = row_topp_bf16(row, V, c, p1.m, p1.z, top_p, smem, s);
+        else tp = row_topp_bisect<T>(row, V, c, p1.m, p1.z, top_p, s);
         st.tau = tp.tau;
         st.n_keep = tp.n_keep;
         st.c_tau = tp.c_tau;
@@ -885,13 +1166,13 @@ __device__ RowStat row_stats(const T* __restrict__ row, int V, float c, float to
         const float xt = st.x_tok;
         if (xt == st.tau && tp.n_keep < tp.c_tau) {
             int before = 0;
-            row_find_nth_equal<T>(row, V, st.tau, 0x7fffffff, tok, &before, s);
+            row_find_nth_equal<T>(row, V, st.tau, -1, tok, &before, s, ss);
             member = before < tp.n_keep;
         } else {
             member = xt >= st.tau;
         }
     }
-    st.inv_zn = 1.0f / (float)mass;
+    st.inv_zn = 1.0f / ff_to_float(mass);
     st.flags = member ? kRowTokMember : 0;
     return st;
 }

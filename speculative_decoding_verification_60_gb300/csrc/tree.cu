@@ -102,25 +102,29 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
     __syncthreads();
 
     int n = 0, dep = 0, t = -1;
-    if (tid < W) {
-        a.path[(size_t)b * W + tid] = (tid == 0) ? 0 : -1;
-        a.out_tokens[(size_t)b * W + tid] = -1;
+    for (int i = tid; i < W; i += kNT) {
+        a.path[(size_t)b * W + i] = (i == 0) ? 0 : -1;
+        a.out_tokens[(size_t)b * W + i] = -1;
     }
     bool inval = sh_inval != 0;
     while (!inval) {
         // children of n, in index order
         {
-            const int i = tid;
-            const bool is_child = (i > n && i < N && a.parent[i] == n);
-            int tot;
-            const int at = block_exclusive_scan_i(is_child ? 1 : 0, s, &tot);
-            if (is_child && at < kMaxChildren) ch[at] = i;
-            if (tid == 0) sh_m = tot;
+            int found = 0;
+            for (int c0 = n + 1; c0 < N; c0 += kNT) {  // children have larger indices than their parent
+                const int i = c0 + tid;
+                const bool is_child = (i < N && a.parent[i] == n);
+                int tot;
+                const int at = found + block_exclusive_scan_i(is_child ? 1 : 0, s, &tot);
+                if (is_child && at < kMaxChildren) ch[at] = i;
+                found += tot;
+            }
+            if (tid == 0) sh_m = found;
             __syncthreads();
         }
         const int m = sh_m;
         const T* prow = tgt + (size_t)n * V;
-        const RowStat sp = row_stats<T, MODE>(prow, V, a.c, a.top_p, -1, topsmem, s);
+        const RowStat sp = row_stats<T, MODE>(prow, V, a.c, a.top_p, -1, topsmem, s, ss);
         if (sp.flags & kRowInvalid) {
             if (tid == 0) atomicOr(&sh_inval, kDevErrNonfinite);
             inval = true;
@@ -146,7 +150,7 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
             continue;
         }
         const RowView<T> rv(prow, V);
-        const FilteredRow<T> P(prow, sp, a.c, nucleus_cut<T>(prow, V, sp, s));
+        const FilteredRow<T> P(prow, sp, a.c, nucleus_cut<T>(prow, V, sp, s, ss));
         const float up = uniform01(a.seed, req, pos + dep + 1, m == 0 ? kPurposeBonus : kPurposeResidual, 0);
         if (m == 0) {
             auto wp = [&](int unit, float* w, int& i0, int& cnt) {
@@ -164,14 +168,14 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
         RowStat sq = sp;
         const T* qrow = drf ? drf + (size_t)n * V : prow;
         if (use_q) {
-            sq = row_stats<T, MODE>(qrow, V, a.c, a.top_p, -1, topsmem, s);
+            sq = row_stats<T, MODE>(qrow, V, a.c, a.top_p, -1, topsmem, s, ss);
             if (sq.flags & kRowInvalid) {
                 if (tid == 0) atomicOr(&sh_inval, kDevErrNonfinite);
                 inval = true;
                 break;
             }
         }
-        const FilteredRow<T> Q(qrow, sq, a.c, use_q ? nucleus_cut<T>(qrow, V, sq, s) : 0x7fffffff);
+        const FilteredRow<T> Q(qrow, sq, a.c, use_q ? nucleus_cut<T>(qrow, V, sq, s, ss) : 0x7fffffff);
         if (tid == 0) R.n = 0;
         __syncthreads();
         int next = -1;
@@ -206,8 +210,8 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
                         w[e] = fmaxf(0.0f, Pv - Qv);
                     }
                 };
-                const double Nj = block_weight_total<VEC>(rv.units(), wres, s);
-                if (tid == 0) R.inv_norm[j] = Nj > 0.0 ? (float)(1.0 / Nj) : 0.0f;
+                const ff Nj = block_weight_total<VEC>(rv.units(), wres, s);
+                if (tid == 0) R.inv_norm[j] = Nj.hi > 0.0f ? 1.0f / ff_to_float(Nj) : 0.0f;
             }
             if (tid == 0) R.n = j + 1;
             __syncthreads();
@@ -240,9 +244,9 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
     if (bad) {
         t = row_argmax_finite<T>(tgt, V, s);
         dep = 0;
-        if (tid < W) {
-            a.path[(size_t)b * W + tid] = (tid == 0) ? 0 : -1;
-            a.out_tokens[(size_t)b * W + tid] = (tid == 0) ? t : -1;
+        for (int i = tid; i < W; i += kNT) {
+            a.path[(size_t)b * W + i] = (i == 0) ? 0 : -1;
+            a.out_tokens[(size_t)b * W + i] = (i == 0) ? t : -1;
         }
     }
     if (tid == 0) {
@@ -282,7 +286,7 @@ extern "C" spec_status spec_verify_tree(const void* target_logits, const void* d
     if (cm != SPEC_CHILD_WOR && cm != SPEC_CHILD_IID && cm != SPEC_CHILD_DETERMINISTIC) return SPEC_ERR_INVALID_ARG;
     const bool greedy = (T == 0.0f);
     if (!greedy && cm != SPEC_CHILD_DETERMINISTIC && !draft_logits) return SPEC_ERR_INVALID_ARG;
-    if ((int64_t)V > kMaxTiles * (int64_t)kNT * 4 - 16) return SPEC_ERR_UNSUPPORTED;
+    if ((int64_t)V > kMaxVocab) return SPEC_ERR_UNSUPPORTED;
     (void)workspace;
     (void)workspace_bytes;
     if (!select_device_of(target_logits)) return SPEC_ERR_INVALID_ARG;
