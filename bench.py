@@ -38,7 +38,7 @@ TREE_WORKLOAD = "tree-b32-n60-k4-d5-v128256"
 HIDDEN = 7168
 METRIC = "verified logit rows/s at V=128256 bf16; achieved HBM GB/s vs GB300 peak"
 UNIT = "rows/s"
-PROFILE = os.path.join(ROOT, "profiles", "k_linear_rowstats_linear-b256-k8-v128256-t0.7-p0.9.md")
+PROFILE = os.path.join(ROOT, "profiles", "k_linear_rowstats_linear-b256-k8-v128256-t0.7-p0.9.txt")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -83,7 +83,10 @@ def recorded_traffic():
     for line in open(PROFILE):
         if ":" in line and line.strip().startswith("- "):
             key, _, val = line.strip()[2:].partition(":")
-            kv[key.strip()] = val.strip().strip("`")
+            val = val.strip()
+            if val.startswith("`") and "`" in val[1:]:
+                val = val[1:val.index("`", 1)]  # the value quoted in backticks; a comment may follow
+            kv[key.strip()] = val
     if kv.get("source_sha") != source_sha():
         return None
     try:

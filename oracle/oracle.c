@@ -28,7 +28,8 @@
  *  - §"MTP" / §"MTP schedule for a single token": token t_{i+1} pairs with
  *    hidden state H_i; a kernel inserts the next tokens into their slots.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent (choices of this oracle, not statements
+ * of the pages):
  *  - temperature T == 0 means greedy (argmax, ties to the lowest index);
  *  - top-p keeps, in (logit desc, index asc) order, each token whose
  *    preceding mass is < top_p; top_p >= 1 disables it;

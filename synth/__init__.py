@@ -6,7 +6,7 @@ holds none of the verification method's arithmetic (no softmax, no
 filtering, no acceptance rule, no sampling from model distributions); both
 the CUDA path and the oracle consume what it returns.
 
-Recipe (each a reading of a workload description; listed in the design doc):
+Recipe (each a reading of a workload description):
   * "Zipf" logits: N(0, 1) plus a bias of 8 * r^-1.1, where r in 1..V is the
     token's rank in an independent random permutation of the vocabulary per
     row (rank 1 gets +8).  Rounded to bf16 once.
