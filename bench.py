@@ -62,6 +62,30 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def shard(rank: int, B: int, data_seed: int) -> dict:
+    """Rank `rank`'s share of the job: B requests with their own ids and data
+    seeds (requests are independent; no rank reads another's rows)."""
+    return {"first_request": rank * B, "data_seed": data_seed + 97 * rank, "draft_seed": 11 + rank,
+            "hidden_seed": data_seed + 1 + rank}
+
+
+def max_over_ranks(values, world: int, device):
+    """Element-wise max of per-rank timings (identity on one rank)."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_value(rows_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the rows of every rank over the slowest rank's step time."""
+    return rows_per_rank * world / (ms / 1e3)
+
+
 def source_sha() -> str:
     """Hash of the kernel sources, to tell whether recorded counters still apply."""
     h = hashlib.sha256()
@@ -194,11 +218,12 @@ class LinearStep:
         self.T, self.top_p, self.seed = w["T"], w["top_p"], w["seed"]
         B, k, V = self.B, self.k, self.V
         self.dev = device
-        self.tgt, self.drf = synth.linear_logits(B, k, V, "bf16", w["data_seed"] + 97 * rank, device=device)
-        self.d = draft_tokens_torch(self.drf, self.T, self.top_p, seed=11 + rank)
-        self.req = (torch.arange(B, dtype=torch.int64, device=device) + rank * B)
+        sh = shard(rank, B, w["data_seed"])
+        self.tgt, self.drf = synth.linear_logits(B, k, V, "bf16", sh["data_seed"], device=device)
+        self.d = draft_tokens_torch(self.drf, self.T, self.top_p, seed=sh["draft_seed"])
+        self.req = (torch.arange(B, dtype=torch.int64, device=device) + sh["first_request"])
         self.pos = torch.full((B,), 1000, dtype=torch.int64, device=device)
-        self.hidden = synth.hidden_states(B, k + 1, HIDDEN, seed=w["data_seed"] + 1 + rank, device=device)
+        self.hidden = synth.hidden_states(B, k + 1, HIDDEN, seed=sh["hidden_seed"], device=device)
         ws = svp.workspace_size(svp.SPEC_OP_LINEAR, B, k, V)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         i32, f32 = torch.int32, torch.float32
@@ -388,17 +413,11 @@ def run_ours(args):
     clocks.start()
     ms, stats_ms, launches = time_linear(step, args.steps, args.warmup, barrier)
     clk = clocks.stop()
-    if world > 1:
-        t = torch.tensor([ms, stats_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, stats_ms = float(t[0]), float(t[1])
-    rows = step.B * (step.k + 1) * world
-    value = rows / (ms / 1e3)
+    ms, stats_ms = max_over_ranks([ms, stats_ms], world, device)
+    rows = step.B * (step.k + 1)
+    value = job_value(rows, world, ms)
     e2e_ms, h2d, d2h = (ms, 0, 0) if args.no_e2e else time_e2e(step, args.e2e_steps)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks([e2e_ms], world, device)[0]
     tree = None if args.no_tree else time_tree(device, max(3, args.steps // 2), 2)
     peak, peak_kind = hbm_peak()
     achieved = step.algo_bytes / (stats_ms / 1e3) / 1e9
@@ -424,7 +443,7 @@ def run_ours(args):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "traffic": recorded_traffic(),
                      "algorithmic_bytes_per_launch": step.algo_bytes, "launch_ms": round(stats_ms, 4)},
-        "e2e": {"value": round(rows / (e2e_ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+        "e2e": {"value": round(job_value(rows, world, e2e_ms), 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk,
