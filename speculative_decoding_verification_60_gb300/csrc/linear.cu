@@ -60,17 +60,14 @@ __global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a) {
     }
 }
 
-// One cluster of kDecCluster CTAs per request: every CTA takes the accept
-// decisions (cheap, identical), the draw is split over the cluster, and CTA 0
-// writes the request's outputs.
+// One CTA per request: warp 0 takes the accept decisions, then the whole
+// CTA draws the residual or bonus token.
 template <typename T, int MODE>
-__global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
+__global__ void __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
     __shared__ BlockScratch s;
-    __shared__ SampleScratch ss;
+    __shared__ DrawScratch ds;
     __shared__ int sh_a, sh_inval;
-    cg::cluster_group cl = cg::this_cluster();
-    const int rank = (int)cl.block_rank();
-    const int b = blockIdx.x / kDecCluster, k = a.k, V = a.V;
+    const int b = blockIdx.x, k = a.k, V = a.V;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t req = a.req ? a.req[b] : (int64_t)b;
     const int64_t pos = a.pos ? a.pos[b] : 0;
@@ -108,7 +105,7 @@ __global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kNT, 2) k_
                     acc = uniform01(a.seed, req, pos + i + 1, kPurposeAccept, 0) < ratio;
                 }
             }
-            if (i < k && rank == 0) {
+            if (i < k) {
                 if (a.accept_prob) a.accept_prob[(size_t)b * k + i] = inval ? 0.0f : ap;
                 if (a.token_probs) {
                     a.token_probs[((size_t)b * k + i) * 2 + 0] = inval ? 0.0f : pp;
@@ -128,7 +125,7 @@ __global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kNT, 2) k_
     const T* tgt = static_cast<const T*>(a.tgt) + (size_t)b * (k + 1) * V;
     int t = -1;
     if (inval) {
-        if (rank == 0) t = row_argmax_finite<T>(tgt, V, s);
+        t = row_argmax_finite<T>(tgt, V, s);
     } else if (MODE == 0) {
         t = a.stats[tgt_row(a, b, acnt)].argmax;
     } else {
@@ -142,15 +139,13 @@ __global__ void __cluster_dims__(kDecCluster, 1, 1) __launch_bounds__(kNT, 2) k_
             const RowStat sq = a.stats[drf_row(a, b, acnt)];
             const T* qrow = static_cast<const T*>(a.drf) + ((size_t)b * k + acnt) * V;
             FilteredRow<T> Q(qrow, sq, a.c, 0x7fffffff);
-            nucleus_cuts<T>(cl, rv, P, &Q, s, ss);
-            t = draw_filtered<T, true, (MODE == 2)>(cl, rv, P, Q, u, s, ss);
-            if (t < 0) t = draw_filtered<T, false, (MODE == 2)>(cl, rv, P, P, u, s, ss);  // p == q: draw from p
+            t = draw_linear<T, true, (MODE == 2)>(rv, P, Q, u, s, ds);
+            if (t < 0) t = draw_linear<T, false, (MODE == 2)>(rv, P, Q, u, s, ds);  // p == q: draw from p
         } else {
-            nucleus_cuts<T>(cl, rv, P, nullptr, s, ss);
-            t = draw_filtered<T, false, (MODE == 2)>(cl, rv, P, P, u, s, ss);
+            t = draw_linear<T, false, (MODE == 2)>(rv, P, P, u, s, ds);
         }
     }
-    if (rank == 0 && threadIdx.x == 0) {
+    if (threadIdx.x == 0) {
         a.acc_len[b] = acnt;
         int32_t* o = a.out_tokens + (size_t)b * (k + 1);
         for (int j = 0; j <= k; ++j) o[j] = (j < acnt) ? d[j] : (j == acnt ? t : -1);
@@ -175,7 +170,7 @@ static spec_status launch_stats(LinearArgs& a, cudaStream_t st) {
 // Stage 2: accept tests, accepted length and the residual / bonus draw.
 template <typename T, int MODE>
 static spec_status launch_decide(LinearArgs& a, cudaStream_t st) {
-    k_linear_finalize<T, MODE><<<a.B * kDecCluster, kNT, 0, st>>>(a);
+    k_linear_finalize<T, MODE><<<a.B, kNT, 0, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -204,7 +204,8 @@ __device__ Pass1 row_pass1(const T* __restrict__ row, int V, float c, BlockScrat
     float x_head = -INFINITY, x_tail = -INFINITY;
 
     if (sample) {
-        for (int i = tid; i < kSampleCap / 8; i += kNT)
+        const int nslots = min(kSampleCap, 2 * kNT * ((rv.nvec + kUnroll * kNT - 1) / (kUnroll * kNT)));
+        for (int i = tid; i < (nslots + 7) / 8; i += kNT)
             reinterpret_cast<uint4*>(sample)[i] = make_uint4(0x7fff7fffu, 0x7fff7fffu, 0x7fff7fffu, 0x7fff7fffu);
         __syncthreads();
     }
@@ -453,6 +454,9 @@ __device__ __forceinline__ int keep_count(ff F, ff pZ, float w, int cnt) {
     else if (n < cnt && ff_lt(ff_two_prod((float)n, w), d)) ++n;
     return n;
 }
+
+// Number of 16-byte vectors of a bf16 row (as RowView counts them).
+__device__ __forceinline__ int rv_nvec(const __nv_bfloat16* row, int V) { return RowView<__nv_bfloat16>(row, V).nvec; }
 
 // Lower bound on the nucleus boundary: a token of weight w <= (1 - top_p) *
 // Z / V cannot be kept (the tail from that token on holds at most V tokens,
@@ -884,7 +888,8 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
         }
         int nv = 0;
         float gb = 0.0f, vb = 0.0f;  // sampled mass (and squares) below tlo
-        for (int i = tid; i < kSampleCap; i += kNT) {
+        const int nslots = min(kSampleCap, 2 * kNT * ((rv_nvec(row, V) + kUnroll * kNT - 1) / (kUnroll * kNT)));
+        for (int i = tid; i < nslots; i += kNT) {
             const uint32_t b = sample[i];
             if ((b & 0x7fffu) > 0x7f80u) continue;  // empty slot
             const float x = bf16_bits_to_float(b);
@@ -916,21 +921,24 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
         // this thread's bins j = kBinsPerThread * tid + i, j ascending from the max:
         // thread maxima at lower-bound weights (tm), sample mass (sm), its squares (sv), counts (sn)
         const int jt = kBinsPerThread * tid;
-        auto bin_vals = [&](int i, float& tmv, float& smv, float& svv, float& snv) {
-            const int j = jt + i;
-            const float jf = (float)j;
-            const uint32_t tc = tcount[j], sc = scount[j];
-            const float wc = ex2(-(jf + 0.5f) * cdl);
-            tmv = tc ? (float)tc * ex2(-(jf + 2.0f) * cdl) : 0.0f;
-            smv = (float)sc * wc;
-            svv = smv * wc;
-            snv = (float)sc;
-        };
+        float tmv[kBinsPerThread], smv[kBinsPerThread], svv[kBinsPerThread], snv[kBinsPerThread];
         float4 own = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-        for (int i = 0; i < kBinsPerThread; ++i) {
-            float a1, a2, a3, a4;
-            bin_vals(i, a1, a2, a3, a4);
-            own.x += a1; own.y += a2; own.z += a3; own.w += a4;
+#pragma unroll
+        for (int i4 = 0; i4 < kBinsPerThread; i4 += 4) {
+            const uint4 tc4 = *reinterpret_cast<const uint4*>(tcount + jt + i4);
+            const uint4 sc4 = *reinterpret_cast<const uint4*>(scount + jt + i4);
+            const uint32_t tca[4] = {tc4.x, tc4.y, tc4.z, tc4.w}, sca[4] = {sc4.x, sc4.y, sc4.z, sc4.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int i = i4 + q;
+                const float jf = (float)(jt + i);
+                const float wc = ex2(-(jf + 0.5f) * cdl);
+                tmv[i] = tca[q] ? (float)tca[q] * ex2(-(jf + 2.0f) * cdl) : 0.0f;
+                smv[i] = (float)sca[q] * wc;
+                svv[i] = smv[i] * wc;
+                snv[i] = (float)sca[q];
+                own.x += tmv[i]; own.y += smv[i]; own.z += svv[i]; own.w += snv[i];
+            }
         }
         // prefixes over bins in j order (four quantities), warp by warp
         float4 inc = own;
@@ -959,14 +967,13 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
         int jp = 0x7fffffff, j0 = -1;
         {
             float rt = pt0, rm = pm0;
+#pragma unroll
             for (int i = 0; i < kBinsPerThread; ++i) {
-                float tmv, smv, svv, snv;
-                bin_vals(i, tmv, smv, svv, snv);
                 const int j = jt + i;
-                rt += tmv;
+                rt += tmv[i];
                 if (jp == 0x7fffffff && rt * lower >= thr_pk) jp = j;
                 if (Gb + (all.y - rm) >= T0) j0 = j;
-                rm += smv;
+                rm += smv[i];
             }
             if (tid == 0 && Gb >= T0) j0 = max(j0, kEstBins);  // the position below tlo
         }
@@ -978,14 +985,13 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
         // the owners of bins Jp + 2 and J0 publish the sample count and the squares there
         {
             float rn = pn0, rv = pv0;
+#pragma unroll
             for (int i = 0; i < kBinsPerThread; ++i) {
-                float tmv, smv, svv, snv;
-                bin_vals(i, tmv, smv, svv, snv);
                 const int j = jt + i;
-                rn += snv;
+                rn += snv[i];
                 if (Jp != 0x7fffffff && j == min(Jp + 2, kEstBins - 1)) s.bcast_f[5] = rn;
                 if (j == J0) s.bcast_f[6] = Vb + (all.z - rv);
-                rv += svv;
+                rv += svv[i];
             }
             if (tid == 0 && J0 == kEstBins) s.bcast_f[6] = Vb;
         }
@@ -1002,14 +1008,13 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
             const float Ta = T0 * (1.0f - eps), Tb = T0 * (1.0f + eps);
             int ja = -1, jb = -1;
             float rm = pm0;
+#pragma unroll
             for (int i = 0; i < kBinsPerThread; ++i) {
-                float tmv, smv, svv, snv;
-                bin_vals(i, tmv, smv, svv, snv);
                 const int j = jt + i;
                 const float G = Gb + (all.y - rm);
                 if (G >= Ta) ja = j;
                 if (G >= Tb) jb = j;
-                rm += smv;
+                rm += smv[i];
             }
             if (tid == 0 && Gb >= Ta) ja = max(ja, kEstBins);
             if (tid == 0 && Gb >= Tb) jb = max(jb, kEstBins);

@@ -11,13 +11,9 @@
 // read, once plus one step.
 #pragma once
 
-#include <cooperative_groups.h>
-
 #include "rowstats.cuh"
 
 namespace sv {
-
-namespace cg = cooperative_groups;
 
 // WeightFn: void operator()(int unit, float* w /*[VEC]*/, int& idx0, int& cnt) const
 // Returns the drawn index, or -1 when every weight is zero.
@@ -271,210 +267,79 @@ __device__ int nucleus_cut(const T* row, int V, const RowStat& st, BlockScratch&
 }
 
 // ------------------------------------------------ linear residual / bonus --
-// The draw of the linear step reads the selected rows from HBM, so it is
-// spread over a cluster of kDecCluster CTAs (one request per cluster) and
-// organised for memory parallelism: a step is kDrawStep consecutive units,
-// lane l takes units l, l + 32, ... of it, and all of a step's loads (for
-// both rows) are issued before any is used.  CTA r of the cluster owns a
-// contiguous quarter of the steps; per-step results meet through
-// distributed shared memory.  Every cluster barrier below is reached by
-// all CTAs of the cluster (the control flow around them is uniform).
-constexpr int kDecCluster = 1;
+// The draw of the linear step reads the selected rows once from HBM.  A step
+// is kDrawStep consecutive units; warp w takes steps w, w + kNW, ... and lane
+// l units l, l + 32, ... of each, with all of a step's loads (both rows)
+// issued before any is used.
+//
+// With top-p, a token whose logit equals the row's boundary value tau is
+// kept only up to the n_keep-th such token in index order (the cut), which
+// is not known before the row is read.  So the first pass sums every step
+// as if all tau-valued tokens were kept, and records per step how much the
+// sum changes when its tau_p-valued tokens, its tau_q-valued tokens, or
+// both, are dropped, and how many there are.  From the counts the cut steps
+// follow; the cut indices and the two cut steps' exact sums come from one
+// re-read of those steps, and every other step's sum is its recorded sum
+// plus the corrections of the cuts it lies past.
 constexpr int kDrawUnitsPerLane = 8;
 constexpr int kDrawStep = 32 * kDrawUnitsPerLane;
 constexpr int kSub = kDrawUnitsPerLane;  // 32-unit sub-steps of a step
-static_assert((long long)(kMaxSteps - 2 * kSub) * kDrawStep >= kMaxRowUnits, "step sums do not cover the largest row");
-static_assert(kSub % kNW == 0 || kNW % kSub == 0, "sub-steps per warp");
+constexpr int kDrawMaxSteps = 1024;
+static_assert((long long)kDrawMaxSteps * kDrawStep >= kMaxRowUnits, "draw steps do not cover the largest row");
 
-struct ClusterSteps {
-    int units, nsteps, lo, hi;  // this CTA's steps [lo, hi)
-    __device__ ClusterSteps(int units_, int rank) : units(units_) {
-        nsteps = (units + kDrawStep - 1) / kDrawStep;
-        const int per = (nsteps + kDecCluster - 1) / kDecCluster;
-        lo = rank * per;
-        hi = min(nsteps, lo + per);
-    }
+struct DrawScratch {
+    float base_h[kDrawMaxSteps], base_l[kDrawMaxSteps];  // step sums, every tau-valued token kept
+    float dp[kDrawMaxSteps];   // change when the step's tau_p-valued tokens are dropped
+    float dq[kDrawMaxSteps];   // ... its tau_q-valued tokens
+    float dpq[kDrawMaxSteps];  // the extra change when both are dropped (tokens tau-valued in both rows)
+    int cp[kDrawMaxSteps], cq[kDrawMaxSteps];
+    float sub_h[kSub], sub_l[kSub];  // per sub-step results of a re-read step
+    int sub_i[kSub], sub_j[kSub];
 };
-
-// Owner CTA of step st.
-__device__ __forceinline__ int step_owner(const ClusterSteps& cs, int st) {
-    const int per = (cs.nsteps + kDecCluster - 1) / kDecCluster;
-    return st / per;
-}
-
-// Last kept boundary-valued index of P and, when Q is given, of Q (INT_MAX
-// when every boundary-valued token is kept), known to every CTA of the
-// cluster on return.  One pass over both rows counts the boundary-valued
-// elements per step; each CTA then locates the n_keep-th one of each row.
-template <typename T>
-__device__ void nucleus_cuts(cg::cluster_group& cl, const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<T>* Q,
-                             BlockScratch& s, SampleScratch& ss) {
-    constexpr int VEC = ElemT<T>::VEC;
-    const bool needP = P.st.tau > -INFINITY && P.st.n_keep < P.st.c_tau;
-    const bool needQ = Q && Q->st.tau > -INFINITY && Q->st.n_keep < Q->st.c_tau;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const ClusterSteps cs(rv.units(), (int)cl.block_rank());
-    int* cp = reinterpret_cast<int*>(ss.sh);
-    int* cq = reinterpret_cast<int*>(ss.sl);
-    const float tp = P.st.tau, tq = Q ? Q->st.tau : 0.0f;
-    auto eq_mask = [&](const uint4& v, float tau, int cnt) -> unsigned {
-        float x[VEC];
-        ElemT<T>::unpack(v, x);
-        unsigned m = 0u;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            if (j < cnt && x[j] == tau) m |= 1u << j;
-        return m;
-    };
-    // elements equal to tau among the unit's 16 bytes (padding is -inf and tau is finite)
-    auto eq_count = [&](const uint4& v, float tau, int cnt) -> int {
-        if constexpr (sizeof(T) == 2) {
-            if (tau != 0.0f) {  // bit equality is value equality away from +-0 (rows hold no NaN)
-                const uint32_t tb = __float_as_uint(tau) >> 16;
-                const uint32_t t2 = tb | (tb << 16);
-                const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-                int n = 0;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint32_t d = w4[j] ^ t2;
-                    n += ((d & 0xffffu) == 0u) + ((d >> 16) == 0u);
-                }
-                return n;
-            }
-        }
-        return __popc(eq_mask(v, tau, cnt));
-    };
-    if (needP || needQ) {
-        for (int st = cs.lo + warp; st < cs.hi; st += kNW) {
-            uint4 vp[kDrawUnitsPerLane], vq[kDrawUnitsPerLane];
-#pragma unroll
-            for (int g = 0; g < kDrawUnitsPerLane; ++g) {
-                const int u = st * kDrawStep + g * 32 + lane;
-                int i0 = 0, cnt = 0;
-                if (u < cs.units) rv.unit_range(u, i0, cnt);
-                vp[g] = (needP && cnt) ? P.raw(i0, cnt) : make_uint4(0u, 0u, 0u, 0u);
-                vq[g] = (needQ && cnt) ? Q->raw(i0, cnt) : make_uint4(0u, 0u, 0u, 0u);
-            }
-            int np = 0, nq = 0;
-#pragma unroll
-            for (int g = 0; g < kDrawUnitsPerLane; ++g) {
-                const int u = st * kDrawStep + g * 32 + lane;
-                int i0 = 0, cnt = 0;
-                if (u < cs.units) rv.unit_range(u, i0, cnt);
-                if (needP) np += eq_count(vp[g], tp, cnt);
-                if (needQ) nq += eq_count(vq[g], tq, cnt);
-            }
-            np = warp_sum_i(np);
-            nq = warp_sum_i(nq);
-            if (lane == 0) {
-                cp[st] = np;
-                cq[st] = nq;
-            }
-        }
-    }
-    cl.sync();
-    // every CTA: the step holding the n-th element (warp 0 over all steps), then
-    // its sub-steps, one warp each
-    auto locate = [&](int which, const FilteredRow<T>& R, int n) -> int {
-        if (warp == 0) {
-            const int per = (cs.nsteps + 31) / 32;
-            int ls = 0;
-            for (int i = 0; i < per; ++i) {
-                const int st = lane * per + i;
-                if (st < cs.nsteps) {
-                    const int* src = cl.map_shared_rank(which ? cq : cp, step_owner(cs, st));
-                    ls += src[st];
-                }
-            }
-            const int incl = warp_inclusive_scan_i(ls);
-            const int total = __shfl_sync(0xffffffffu, incl, 31);
-            int js = -1, pre = 0;
-            if (n >= 0 && n < total) {
-                const unsigned bal = __ballot_sync(0xffffffffu, incl > n);
-                const int L = __ffs(bal) - 1;
-                if (lane == L) {
-                    int run = incl - ls;
-                    for (int i = 0; i < per; ++i) {
-                        const int st = lane * per + i;
-                        const int* src = cl.map_shared_rank(which ? cq : cp, step_owner(cs, st));
-                        if (run + src[st] > n) { js = st; pre = run; break; }
-                        run += src[st];
-                    }
-                }
-                js = __shfl_sync(0xffffffffu, js, L);
-                pre = __shfl_sync(0xffffffffu, pre, L);
-            }
-            if (lane == 0) { s.bcast_i[0] = js; s.bcast_i[1] = pre; }
-        }
-        __syncthreads();
-        const int js = s.bcast_i[0];
-        int pre = s.bcast_i[1];
-        __syncthreads();
-        if (js < 0) return 0x7fffffff;
-        int* subc = reinterpret_cast<int*>(s.pf3);  // kSub counts (kSub <= kNW)
-        unsigned msk = 0u;
-        int i0 = 0;
-        const int g = warp;
-        if (g < kSub) {
-            const int u = js * kDrawStep + g * 32 + lane;
-            int cnt = 0;
-            if (u < cs.units) rv.unit_range(u, i0, cnt);
-            msk = cnt ? eq_mask(R.raw(i0, cnt), R.st.tau, cnt) : 0u;
-            const int c = warp_sum_i(__popc(msk));
-            if (lane == 0) subc[g] = c;
-        }
-        __syncthreads();
-        int base = pre, gsel = -1, gpre = 0;
-        for (int gg = 0; gg < kSub; ++gg) {
-            if (gsel < 0 && base + subc[gg] > n) { gsel = gg; gpre = base; }
-            base += subc[gg];
-        }
-        if (threadIdx.x == 0) s.bcast_i[2] = 0x7fffffff;
-        __syncthreads();
-        if (g == gsel) {
-            const int c = __popc(msk);
-            const int ic = warp_inclusive_scan_i(c);
-            if (gpre + ic > n && gpre + ic - c <= n) {
-                int kk = n - (gpre + ic - c);
-                for (int j = 0; j < VEC; ++j)
-                    if (msk & (1u << j)) {
-                        if (kk == 0) { s.bcast_i[2] = i0 + j; break; }
-                        --kk;
-                    }
-            }
-        }
-        __syncthreads();
-        const int r = s.bcast_i[2];
-        __syncthreads();
-        return r;
-    };
-    static_assert(kSub <= kNW, "one sub-step per warp in the locate");
-    P.cut = needP ? locate(0, P, P.st.n_keep - 1) : 0x7fffffff;
-    if (Q) Q->cut = needQ ? locate(1, *Q, Q->st.n_keep - 1) : 0x7fffffff;
-    cl.sync();  // the counts may be overwritten from here on
-}
 
 // Inverse-CDF draw over the units of rv with weights max(0, p - q) (RESID)
 // or p: the smallest v with C(v) > u * C(last), C the running sum in index
-// order.  Returns, in every CTA of the cluster, the drawn index or -1 when
-// every weight is zero.
+// order.  P and Q carry their rows' statistics; on return their cuts are
+// set.  Returns -1 when every weight is zero.
 template <typename T, bool RESID, bool TOPP>
-__device__ int draw_filtered(cg::cluster_group& cl, const RowView<T>& rv, const FilteredRow<T>& P,
-                             const FilteredRow<T>& Q, float u, BlockScratch& s, SampleScratch& ss) {
+__device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<T>& Q, float u, BlockScratch& s,
+                           DrawScratch& ds) {
     constexpr int VEC = ElemT<T>::VEC;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int rank = (int)cl.block_rank();
-    const ClusterSteps cs(rv.units(), rank);
-    auto weights = [&](const uint4& rp, const uint4& rq, int i0, int cnt, float* w) -> float {
-        P.template probs_fast<TOPP>(rp, i0, cnt, w);
-        if (RESID) {
-            float q[VEC];
-            Q.template probs_fast<TOPP>(rq, i0, cnt, q);
+    const int units = rv.units();
+    const int nsteps = (units + kDrawStep - 1) / kDrawStep;
+    const bool needP = TOPP && P.st.tau > -INFINITY && P.st.n_keep < P.st.c_tau;
+    const bool needQ = TOPP && RESID && Q.st.tau > -INFINITY && Q.st.n_keep < Q.st.c_tau;
+    const float tp = P.st.tau, tq = Q.st.tau;
+    P.cut = 0x7fffffff;
+    Q.cut = 0x7fffffff;
+    // weights with the current cuts; also the tau masks of the unit (bit j: element j is tau-valued)
+    auto weights = [&](const uint4& rp, const uint4& rq, int i0, int cnt, float* w, float* pw, unsigned& mp,
+                       unsigned& mq) -> float {
+        P.template probs_fast<TOPP>(rp, i0, cnt, pw);
+        float q[VEC];
+        if (RESID) Q.template probs_fast<TOPP>(rq, i0, cnt, q);
+        mp = 0u;
+        mq = 0u;
+        if (needP || needQ) {
+            float xp[VEC], xq[VEC];
+            ElemT<T>::unpack(rp, xp);
+            if (RESID) ElemT<T>::unpack(rq, xq);
 #pragma unroll
-            for (int j = 0; j < VEC; j += 2) {
-                const float2 d = __fadd2_rn(make_float2(w[j], w[j + 1]), make_float2(-q[j], -q[j + 1]));
+            for (int j = 0; j < VEC; ++j) {
+                if (needP && xp[j] == tp) mp |= 1u << j;
+                if (needQ && xq[j] == tq) mq |= 1u << j;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < VEC; j += 2) {
+            if (RESID) {
+                const float2 d = __fadd2_rn(make_float2(pw[j], pw[j + 1]), make_float2(-q[j], -q[j + 1]));
                 w[j] = fmaxf(0.0f, d.x);
                 w[j + 1] = fmaxf(0.0f, d.y);
+            } else {
+                w[j] = pw[j];
+                w[j + 1] = pw[j + 1];
             }
         }
         float2 a2 = make_float2(0.0f, 0.0f);
@@ -482,43 +347,190 @@ __device__ int draw_filtered(cg::cluster_group& cl, const RowView<T>& rv, const 
         for (int j = 0; j < VEC; j += 2) a2 = __fadd2_rn(a2, make_float2(w[j], w[j + 1]));
         return a2.x + a2.y;
     };
-    // A: this CTA's step sums
-    for (int st = cs.lo + warp; st < cs.hi; st += kNW) {
+    auto unit_of = [&](int st, int g, int& i0, int& cnt) {
+        const int uu = st * kDrawStep + g * 32 + lane;
+        i0 = 0;
+        cnt = 0;
+        if (uu < units) rv.unit_range(uu, i0, cnt);
+    };
+    // A: per-step sums with every tau-valued token kept, corrections and counts
+    for (int st = warp; st < nsteps; st += kNW) {
         uint4 vp[kDrawUnitsPerLane], vq[kDrawUnitsPerLane];
 #pragma unroll
         for (int g = 0; g < kDrawUnitsPerLane; ++g) {
-            const int uu = st * kDrawStep + g * 32 + lane;
-            int i0 = 0, cnt = 0;
-            if (uu < cs.units) rv.unit_range(uu, i0, cnt);
+            int i0, cnt;
+            unit_of(st, g, i0, cnt);
             vp[g] = cnt ? P.raw(i0, cnt) : make_uint4(0u, 0u, 0u, 0u);
             vq[g] = (RESID && cnt) ? Q.raw(i0, cnt) : make_uint4(0u, 0u, 0u, 0u);
         }
-        float a = 0.0f;
+        float a = 0.0f, dp = 0.0f, dq = 0.0f, dpq = 0.0f;
+        int np = 0, nq = 0;
 #pragma unroll
         for (int g = 0; g < kDrawUnitsPerLane; ++g) {
-            const int uu = st * kDrawStep + g * 32 + lane;
-            int i0 = 0, cnt = 0;
-            if (uu < cs.units) rv.unit_range(uu, i0, cnt);
-            float w[VEC];
-            if (cnt) a += weights(vp[g], vq[g], i0, cnt, w);
+            int i0, cnt;
+            unit_of(st, g, i0, cnt);
+            if (!cnt) continue;
+            float w[VEC], pw[VEC];
+            unsigned mp, mq;
+            a += weights(vp[g], vq[g], i0, cnt, w, pw, mp, mq);
+            if (mp | mq) {  // rare: tau-valued tokens in this unit
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const bool ip = (mp >> j) & 1u, iq = (mq >> j) & 1u;
+                    if (ip) dp -= w[j];            // p dropped: max(0, 0 - q) = 0
+                    if (iq) dq += pw[j] - w[j];    // q dropped: max(0, p - 0) = p
+                    if (ip && iq) dpq += w[j] - pw[j];  // both dropped: 0
+                }
+                np += __popc(mp);
+                nq += __popc(mq);
+            }
         }
         const ff t = warp_sum_ff(ff_from(a));
+        dp = warp_sum_f(dp);
+        dq = warp_sum_f(dq);
+        dpq = warp_sum_f(dpq);
+        np = warp_sum_i(np);
+        nq = warp_sum_i(nq);
         if (lane == 0) {
-            ss.sh[st] = t.hi;
-            ss.sl[st] = t.lo;
+            ds.base_h[st] = t.hi;
+            ds.base_l[st] = t.lo;
+            ds.dp[st] = dp;
+            ds.dq[st] = dq;
+            ds.dpq[st] = dpq;
+            ds.cp[st] = np;
+            ds.cq[st] = nq;
         }
     }
-    cl.sync();
-    // B: every CTA finds the crossing step from all step sums (warp 0)
+    __syncthreads();
+    // B1: the steps holding the cuts (warp 0): the n_keep-th tau-valued token of each row
     if (warp == 0) {
-        const int per = (cs.nsteps + 31) / 32;
+        auto cut_step = [&](const int* cnts, int n, int& js, int& pre) {
+            js = -1;
+            pre = 0;
+            const int per = (nsteps + 31) / 32;
+            int ls = 0;
+            for (int i = 0; i < per; ++i) {
+                const int st = lane * per + i;
+                if (st < nsteps) ls += cnts[st];
+            }
+            const int incl = warp_inclusive_scan_i(ls);
+            const int total = __shfl_sync(0xffffffffu, incl, 31);
+            if (n < 0 || n >= total) return;  // every tau-valued token kept
+            const unsigned bal = __ballot_sync(0xffffffffu, incl > n);
+            const int L = __ffs(bal) - 1;
+            if (lane == L) {
+                int run = incl - ls;
+                for (int i = 0; i < per; ++i) {
+                    const int st = lane * per + i;
+                    if (run + cnts[st] > n) { js = st; pre = run; break; }
+                    run += cnts[st];
+                }
+            }
+            js = __shfl_sync(0xffffffffu, js, L);
+            pre = __shfl_sync(0xffffffffu, pre, L);
+        };
+        int jsp = -1, prep = 0, jsq = -1, preq = 0;
+        if (needP) cut_step(ds.cp, P.st.n_keep - 1, jsp, prep);
+        if (needQ) cut_step(ds.cq, Q.st.n_keep - 1, jsq, preq);
+        if (lane == 0) {
+            s.bcast_i[0] = jsp;
+            s.bcast_i[1] = prep;
+            s.bcast_i[2] = jsq;
+            s.bcast_i[3] = preq;
+        }
+    }
+    __syncthreads();
+    const int jsp = s.bcast_i[0], prep = s.bcast_i[1], jsq = s.bcast_i[2], preq = s.bcast_i[3];
+    __syncthreads();
+    // B2: the cut index inside its step, one 32-unit sub-step per warp
+    auto locate = [&](int js, int pre, int n, const FilteredRow<T>& R, float tau) -> int {
+        unsigned msk = 0u;
+        int i0 = 0, cnt = 0;
+        if (warp < kSub) {
+            unit_of(js, warp, i0, cnt);
+            if (cnt) {
+                float x[VEC];
+                ElemT<T>::unpack(R.raw(i0, cnt), x);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    if (j < cnt && x[j] == tau) msk |= 1u << j;
+            }
+            const int c = warp_sum_i(__popc(msk));
+            if (lane == 0) ds.sub_i[warp] = c;
+        }
+        if (threadIdx.x == 0) s.bcast_i[4] = 0x7fffffff;
+        __syncthreads();
+        int base = pre, gsel = -1, gpre = 0;
+        for (int g = 0; g < kSub; ++g) {
+            if (gsel < 0 && base + ds.sub_i[g] > n) { gsel = g; gpre = base; }
+            base += ds.sub_i[g];
+        }
+        if (warp == gsel) {
+            const int c = __popc(msk);
+            const int ic = warp_inclusive_scan_i(c);
+            if (gpre + ic > n && gpre + ic - c <= n) {
+                int kk = n - (gpre + ic - c);
+                for (int j = 0; j < VEC; ++j)
+                    if (msk & (1u << j)) {
+                        if (kk == 0) { s.bcast_i[4] = i0 + j; break; }
+                        --kk;
+                    }
+            }
+        }
+        __syncthreads();
+        const int r = s.bcast_i[4];
+        __syncthreads();
+        return r;
+    };
+    if (jsp >= 0) P.cut = locate(jsp, prep, P.st.n_keep - 1, P, tp);
+    if (jsq >= 0) Q.cut = locate(jsq, preq, Q.st.n_keep - 1, Q, tq);
+    // B3: exact sums of the cut steps (with the cuts now known), one sub-step per warp
+    auto exact_step = [&](int js) -> ff {
+        if (warp < kSub) {
+            int i0, cnt;
+            unit_of(js, warp, i0, cnt);
+            float a = 0.0f;
+            if (cnt) {
+                float w[VEC], pw[VEC];
+                unsigned mp, mq;
+                a = weights(P.raw(i0, cnt), RESID ? Q.raw(i0, cnt) : make_uint4(0u, 0u, 0u, 0u), i0, cnt, w, pw, mp,
+                            mq);
+            }
+            const ff t = warp_sum_ff(ff_from(a));
+            if (lane == 0) {
+                ds.sub_h[warp] = t.hi;
+                ds.sub_l[warp] = t.lo;
+            }
+        }
+        __syncthreads();
+        ff r = ff{0.0f, 0.0f};
+        for (int g = 0; g < kSub; ++g) r = ff_add(r, ff{ds.sub_h[g], ds.sub_l[g]});
+        __syncthreads();
+        return r;
+    };
+    const ff exact_p = (jsp >= 0) ? exact_step(jsp) : ff{0.0f, 0.0f};
+    const ff exact_q = (jsq >= 0 && jsq != jsp) ? exact_step(jsq) : exact_p;
+    // the true sum of step st
+    auto step_sum = [&](int st) -> ff {
+        if (st == jsp) return exact_p;
+        if (st == jsq) return exact_q;
+        ff v = ff{ds.base_h[st], ds.base_l[st]};
+        const bool past_p = jsp >= 0 && st > jsp, past_q = jsq >= 0 && st > jsq;
+        float d = 0.0f;
+        if (past_p) d += ds.dp[st];
+        if (past_q) d += ds.dq[st];
+        if (past_p && past_q) d += ds.dpq[st];
+        return d != 0.0f ? ff_add_f(v, d) : v;
+    };
+    // B4: the crossing step (warp 0)
+    if (warp == 0) {
+        const int per = (nsteps + 31) / 32;
         ff ls = ff{0.0f, 0.0f};
         int lastpos = -1;
         for (int i = 0; i < per; ++i) {
             const int st = lane * per + i;
-            if (st < cs.nsteps) {
-                const int o = step_owner(cs, st);
-                const ff sv = ff{cl.map_shared_rank(ss.sh, o)[st], cl.map_shared_rank(ss.sl, o)[st]};
+            if (st < nsteps) {
+                const ff sv = step_sum(st);
                 ls = ff_add(ls, sv);
                 if (sv.hi > 0.0f) lastpos = st;
             }
@@ -540,9 +552,8 @@ __device__ int draw_filtered(cg::cluster_group& cl, const RowView<T>& rv, const 
                     ff run = before;
                     for (int i = 0; i < per; ++i) {
                         const int st = lane * per + i;
-                        if (st >= cs.nsteps) break;
-                        const int o = step_owner(cs, st);
-                        const ff sv = ff{cl.map_shared_rank(ss.sh, o)[st], cl.map_shared_rank(ss.sl, o)[st]};
+                        if (st >= nsteps) break;
+                        const ff sv = step_sum(st);
                         const ff nx = ff_add(run, sv);
                         if (sv.hi > 0.0f && ff_lt(tgt, nx)) { js = st; pre = run; break; }
                         run = nx;
@@ -558,74 +569,62 @@ __device__ int draw_filtered(cg::cluster_group& cl, const RowView<T>& rv, const 
             }
         }
         if (lane == 0) {
-            s.bcast_i[4] = js;
+            s.bcast_i[5] = js;
             s.bcast_f[0] = pre.hi;
             s.bcast_f[1] = pre.lo;
             s.bcast_f[2] = tgt.hi;
             s.bcast_f[3] = tgt.lo;
         }
     }
-    cl.sync();  // every CTA has read the step sums
-    const int js = s.bcast_i[4];
-    if (js < 0) return -1;  // uniform across the cluster
-    // C: warp g takes sub-steps g, g + kNW, ... (32 units each) of step js
-    constexpr int KW = (kSub + kNW - 1) / kNW;
-    float* sub_h = ss.sh;  // free again after the cluster barrier
-    float* sub_l = ss.sl;
-    int* sub_last = reinterpret_cast<int*>(ss.sh + kSub);
-    float w[KW][VEC];
-    float a_own[KW];
-    int i0s[KW], cnts[KW];
+    __syncthreads();
+    const int js = s.bcast_i[5];
+    const ff tgt = ff{s.bcast_f[2], s.bcast_f[3]};
+    ff run = ff{s.bcast_f[0], s.bcast_f[1]};
+    __syncthreads();
+    if (js < 0) return -1;  // every weight is zero
+    // C: the crossing step, one sub-step per warp
+    float w[VEC];
+    float a_own = 0.0f;
+    int i0 = 0, cnt = 0;
 #pragma unroll
-    for (int k2 = 0; k2 < KW; ++k2) {
-        const int g = warp + k2 * kNW;
-        a_own[k2] = 0.0f;
-        i0s[k2] = 0;
-        cnts[k2] = 0;
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) w[k2][j] = 0.0f;
-        if (g >= kSub) continue;
-        const int uu = js * kDrawStep + g * 32 + lane;
-        int i0 = 0, cnt = 0;
-        if (uu < cs.units) rv.unit_range(uu, i0, cnt);
-        if (cnt) a_own[k2] = weights(P.raw(i0, cnt), RESID ? Q.raw(i0, cnt) : make_uint4(0u, 0u, 0u, 0u), i0, cnt, w[k2]);
-        i0s[k2] = i0;
-        cnts[k2] = cnt;
-        const ff t = warp_sum_ff(ff_from(a_own[k2]));
+    for (int j = 0; j < VEC; ++j) w[j] = 0.0f;
+    if (warp < kSub) {
+        unit_of(js, warp, i0, cnt);
+        if (cnt) {
+            float pw[VEC];
+            unsigned mp, mq;
+            a_own = weights(P.raw(i0, cnt), RESID ? Q.raw(i0, cnt) : make_uint4(0u, 0u, 0u, 0u), i0, cnt, w, pw, mp, mq);
+        }
+        const ff t = warp_sum_ff(ff_from(a_own));
         int mylast = -1;
 #pragma unroll
         for (int j = 0; j < VEC; ++j)
-            if (j < cnt && w[k2][j] > 0.0f) mylast = i0 + j;
+            if (j < cnt && w[j] > 0.0f) mylast = i0 + j;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mylast = max(mylast, __shfl_xor_sync(0xffffffffu, mylast, o));
         if (lane == 0) {
-            sub_h[g] = t.hi;
-            sub_l[g] = t.lo;
-            sub_last[g] = mylast;
+            ds.sub_h[warp] = t.hi;
+            ds.sub_l[warp] = t.lo;
+            ds.sub_j[warp] = mylast;
         }
     }
     __syncthreads();
-    const ff tgt = ff{s.bcast_f[2], s.bcast_f[3]};
-    ff run = ff{s.bcast_f[0], s.bcast_f[1]};
     int g_cross = -1, lastw = -1;
     ff pre_cross = run;
     for (int g = 0; g < kSub; ++g) {  // the same order in every warp
-        const ff sv = ff{sub_h[g], sub_l[g]};
+        const ff sv = ff{ds.sub_h[g], ds.sub_l[g]};
         const ff nx = ff_add(run, sv);
-        if (sub_last[g] >= 0) lastw = sub_last[g];
+        if (ds.sub_j[g] >= 0) lastw = ds.sub_j[g];
         if (g_cross < 0 && sv.hi > 0.0f && ff_lt(tgt, nx)) { g_cross = g; pre_cross = run; }
         run = nx;
     }
-    if (threadIdx.x == 0 && g_cross < 0) s.bcast_i[7] = lastw;  // otherwise the crossing warp writes it
-#pragma unroll
-    for (int k2 = 0; k2 < KW; ++k2) {
-        const int g = warp + k2 * kNW;
-        if (g != g_cross) continue;  // warp-uniform
-        const ff ia = warp_inclusive_scan_ff(ff_from(a_own[k2]));
+    if (threadIdx.x == 0 && g_cross < 0) s.bcast_i[6] = lastw;  // otherwise the crossing warp writes it
+    if (warp == g_cross) {
+        const ff ia = warp_inclusive_scan_ff(ff_from(a_own));
         const ff ua = ff_shfl_up(ia, 1);
         const ff ex = ff_add(pre_cross, lane == 0 ? ff{0.0f, 0.0f} : ua);
-        const unsigned cb = __ballot_sync(0xffffffffu, a_own[k2] > 0.0f && ff_lt(tgt, ff_add(ex, ff_from(a_own[k2]))));
-        int p = sub_last[g];  // rounding: the last weighted element of this sub-step
+        const unsigned cb = __ballot_sync(0xffffffffu, a_own > 0.0f && ff_lt(tgt, ff_add(ex, ff_from(a_own))));
+        int p = ds.sub_j[g_cross];  // rounding: the last weighted element of this sub-step
         if (cb) {
             const int L = __ffs(cb) - 1;
             int q = -1;
@@ -633,19 +632,19 @@ __device__ int draw_filtered(cg::cluster_group& cl, const RowView<T>& rv, const 
                 ff rr = ex;
                 int mylast = -1;
                 for (int j = 0; j < VEC && q < 0; ++j) {
-                    if (j >= cnts[k2]) break;
-                    if (w[k2][j] > 0.0f) mylast = i0s[k2] + j;
-                    rr = ff_add_f(rr, w[k2][j]);
-                    if (w[k2][j] > 0.0f && ff_lt(tgt, rr)) q = i0s[k2] + j;
+                    if (j >= cnt) break;
+                    if (w[j] > 0.0f) mylast = i0 + j;
+                    rr = ff_add_f(rr, w[j]);
+                    if (w[j] > 0.0f && ff_lt(tgt, rr)) q = i0 + j;
                 }
                 if (q < 0) q = mylast;
             }
             p = __shfl_sync(0xffffffffu, q, L);
         }
-        if (lane == 0) s.bcast_i[7] = p;
+        if (lane == 0) s.bcast_i[6] = p;
     }
     __syncthreads();
-    const int r = s.bcast_i[7];
+    const int r = s.bcast_i[6];
     __syncthreads();
     return r;
 }
