@@ -49,6 +49,23 @@ __device__ __forceinline__ float uniform01(uint64_t seed, int64_t req, int64_t p
     return (float)(o.x >> 8) * (1.0f / 16777216.0f);
 }
 
+// ------------------------------------------------------- cached loads --
+// 16-byte read-only load marked evict-first in L2: for a second read of data
+// that is not read again, so that the lines still awaiting their second read
+// stay.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint4 ldg_last_use(const uint4* p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(pol));
+    return v;
+}
+
 // ------------------------------------------------------------- numerics --
 // 2^x on the MUFU unit (flushes results below 2^-126 to zero).
 __device__ __forceinline__ float ex2(float x) {

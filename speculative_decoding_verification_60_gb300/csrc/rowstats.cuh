@@ -748,12 +748,13 @@ __device__ ff band_pass(const __nv_bfloat16* __restrict__ row, int V, float c, f
     if (tid < rv.head) take_scalar(*reinterpret_cast<const unsigned short*>(row + tid));
     const uint4* vp = rv.vec();
     constexpr int kU2 = 4;  // the re-read comes from L2: fewer vectors in flight suffice
+    const uint64_t last_use = l2_evict_first_policy();  // the row's last read
     for (int base_v = tid; base_v < rv.nvec; base_v += kU2 * kNT) {
         uint4 v[kU2];
 #pragma unroll
         for (int u = 0; u < kU2; ++u) {
             const int vi = base_v + u * kNT;
-            v[u] = (vi < rv.nvec) ? __ldg(vp + vi) : neg_inf_vec<__nv_bfloat16>();
+            v[u] = (vi < rv.nvec) ? ldg_last_use(vp + vi, last_use) : neg_inf_vec<__nv_bfloat16>();
         }
         float bsum = 0.0f;
 #pragma unroll
