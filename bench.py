@@ -385,7 +385,9 @@ def time_tree(device, K: int, W: int):
     tok = torch.zeros(B, N, dtype=torch.int32, device=device)
     par = torch.as_tensor(parent, dtype=torch.long, device=device)
     flat = drf[:, par[1:]].reshape(B * (N - 1), V).float() / w["T"]
-    tok[:, 1:] = torch.multinomial(torch.softmax(flat, -1), 1).reshape(B, N - 1).to(torch.int32)
+    g = torch.Generator(device=device)
+    g.manual_seed(w["data_seed"] + 5)
+    tok[:, 1:] = torch.multinomial(torch.softmax(flat, -1), 1, generator=g).reshape(B, N - 1).to(torch.int32)
     parent_d = torch.as_tensor(parent, dtype=torch.int32, device=device)
     out = None
     for _ in range(W):
