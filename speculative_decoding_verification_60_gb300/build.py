@@ -12,7 +12,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["api.cu", "linear.cu", "tree.cu", "compact.cu"]
+SOURCES = ["api.cu", "linear.cu", "decide.cu", "tree.cu", "compact.cu"]
+# threads per CTA of the row-level kernels in each unit (see common.cuh)
+CTA_THREADS = {"decide.cu": 512, "tree.cu": 512}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 
@@ -44,7 +46,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         o = os.path.join(BUILD, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, s):
-            jobs.append([nvcc, *ARCH, *FLAGS, *extra_flags, "-c", s, "-o", o])
+            nt = [f"-DSV_NT={CTA_THREADS[src]}"] if src in CTA_THREADS else []
+            jobs.append([nvcc, *ARCH, *FLAGS, *nt, *extra_flags, "-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)

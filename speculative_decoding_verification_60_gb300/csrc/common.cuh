@@ -11,7 +11,13 @@
 
 namespace sv {
 
-constexpr int kNT = 256;             // threads of every row-level CTA
+// Threads of a row-level CTA.  Each translation unit may set its own (the
+// build passes -DSV_NT); device code is compiled per unit, so the sizes do
+// not meet.
+#ifndef SV_NT
+#define SV_NT 256
+#endif
+constexpr int kNT = SV_NT;
 constexpr int kNW = kNT / 32;        // warps of such a CTA
 constexpr int kPurposeAccept = 1;
 constexpr int kPurposeResidual = 2;

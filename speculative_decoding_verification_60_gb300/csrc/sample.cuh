@@ -281,7 +281,7 @@ __device__ int nucleus_cut(const T* row, int V, const RowStat& st, BlockScratch&
 // follow; the cut indices and the two cut steps' exact sums come from one
 // re-read of those steps, and every other step's sum is its recorded sum
 // plus the corrections of the cuts it lies past.
-constexpr int kDrawUnitsPerLane = 8;
+constexpr int kDrawUnitsPerLane = kNT <= 256 ? 8 : 4;  // fewer registers for larger CTAs
 constexpr int kDrawStep = 32 * kDrawUnitsPerLane;
 constexpr int kSub = kDrawUnitsPerLane;  // 32-unit sub-steps of a step
 constexpr int kDrawMaxSteps = 1024;
