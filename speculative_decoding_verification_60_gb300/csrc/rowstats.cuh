@@ -787,53 +787,60 @@ struct MixedLayout {
 
 // Second pass for a bracket spanning zero (layout above): exact mass above
 // t_b, exact mass of the lump, exact counts of the other keys inside.
+// Branch-free per element: the count goes through one predicated shared
+// reduction at a position computed for every element.
 __device__ inline void band_pass_mixed(const __nv_bfloat16* __restrict__ row, int V, float c, float mc,
                                        const MixedLayout& L, uint32_t* hist, ff& above, ff& lump) {
     const RowView<__nv_bfloat16> rv(row, V);
     const int tid = threadIdx.x;
     const float t_a = key_value(L.key_a), t_b = key_value(L.key_b);
     const float s0 = 0.0009765625f;  // 2^-10
-    auto take = [&](uint32_t b, float x, float w, float& fa, float& fl) {
-        if (x > t_b) {
-            fa += w;
-        } else if (x >= t_a) {
-            const int k = (int)okey16(b);
-            int idx;
-            if (k >= kLumpPosKey) idx = L.key_b - k;
-            else if (k > kLumpNegKey) idx = L.Wp, fl += w;
-            else idx = L.Wp + 1 + (L.kn_top - k);
-            atomicAdd(&hist[idx], 1u);
-        }
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(hist);
+    const int pos_top = L.key_b, lump_pos = L.Wp, neg_top = L.Wp + 1 + L.kn_top;
+    // one element: its exponent argument, its lump weight share, and its count
+    auto take = [&](uint32_t b, float& fa, float& fl) {
+        const float x = bf16_bits_to_float(b);
+        const int k = (int)okey16(b);
+        const bool in_band = (x >= t_a) && (x <= t_b);
+        const bool in_lump = fabsf(x) < s0;
+        const bool abv = x > t_b;
+        const int idx = (k >= kLumpPosKey) ? pos_top - k : (in_lump ? lump_pos : neg_top - k);
+        const float w = ex2((abv || (in_band && in_lump)) ? fmaf(x, c, -mc) : -INFINITY);
+        fa += abv ? w : 0.0f;
+        fl += (in_band && in_lump) ? w : 0.0f;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p red.shared.add.u32 [%0], 1;\n\t}"
+            ::"r"(base + 4u * (uint32_t)idx), "r"((uint32_t)in_band)
+            : "memory");
     };
     float fa = 0.0f, fl = 0.0f, ca = 0.0f;
-    auto weight_if = [&](float x) { return (x > t_b || fabsf(x) < s0) ? weight_of(x, c, mc) : 0.0f; };
-    if (tid < rv.head) {
-        const uint32_t b = *reinterpret_cast<const unsigned short*>(row + tid);
-        const float x = bf16_bits_to_float(b);
-        take(b, x, weight_if(x), fa, fl);
-    }
+    if (tid < rv.head) take(*reinterpret_cast<const unsigned short*>(row + tid), fa, fl);
     const uint4* vp = rv.vec();
-    for (int vi = tid; vi < rv.nvec; vi += kNT) {
-        const uint4 v = __ldg(vp + vi);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+    const uint64_t last_use = l2_evict_first_policy();
+    constexpr int kU2 = 4;
+    for (int base_v = tid; base_v < rv.nvec; base_v += kU2 * kNT) {
+        uint4 v[kU2];
+#pragma unroll
+        for (int u = 0; u < kU2; ++u) {
+            const int vi = base_v + u * kNT;
+            v[u] = (vi < rv.nvec) ? ldg_last_use(vp + vi, last_use) : neg_inf_vec<__nv_bfloat16>();
+        }
         float ba = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t lo = w4[j] & 0xffffu, hi = w4[j] >> 16;
-            const float xl = bf16_bits_to_float(lo), xh = bf16_bits_to_float(hi);
-            take(lo, xl, weight_if(xl), ba, fl);
-            take(hi, xh, weight_if(xh), ba, fl);
+        for (int u = 0; u < kU2; ++u) {
+            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                take(w4[j] & 0xffffu, ba, fl);
+                take(w4[j] >> 16, ba, fl);
+            }
         }
-        const float y = ba - ca;  // Kahan across vectors
+        const float y = ba - ca;  // Kahan across batches
         const float t = fa + y;
         ca = (t - fa) - y;
         fa = t;
     }
-    if (tid < rv.tail) {
-        const uint32_t b = *reinterpret_cast<const unsigned short*>(row + rv.head + rv.nvec * 8 + tid);
-        const float x = bf16_bits_to_float(b);
-        take(b, x, weight_if(x), fa, fl);
-    }
+    if (tid < rv.tail) take(*reinterpret_cast<const unsigned short*>(row + rv.head + rv.nvec * 8 + tid), fa, fl);
     above = ff_add(ff{fa, 0.0f}, ff{-ca, 0.0f});
     lump = ff{fl, 0.0f};
 }
