@@ -116,66 +116,43 @@ __device__ __forceinline__ float batch_weight_sum<float>(const uint4* v, float c
     return acc;
 }
 
-// Merge of two (max, rescaled sum, lowest argmax, NaN) partials.
-struct P1Part {
-    float m;
-    ff z;
-    int idx;
-    int bad;
-};
-template <bool kSum>
-__device__ __forceinline__ P1Part merge_p1(const P1Part& a, const P1Part& b, float c) {
-    P1Part r;
-    r.m = fmaxf(a.m, b.m);
-    if (kSum) {
-        const ff za = (a.m > -INFINITY) ? ff_scale(a.z, ex2((a.m - r.m) * c)) : ff{0.0f, 0.0f};
-        const ff zb = (b.m > -INFINITY) ? ff_scale(b.z, ex2((b.m - r.m) * c)) : ff{0.0f, 0.0f};
-        r.z = ff_add(za, zb);
-    } else {
-        r.z = ff{0.0f, 0.0f};
-    }
-    r.idx = (a.m == b.m) ? min(a.idx, b.idx) : (a.m > b.m ? a.idx : b.idx);
-    r.bad = a.bad | b.bad;
-    return r;
-}
-template <bool kSum>
-__device__ __forceinline__ P1Part shfl_merge_p1(P1Part p, int o, float c) {
-    P1Part q;
-    q.m = __shfl_xor_sync(0xffffffffu, p.m, o);
-    q.z = ff_shfl_xor(p.z, o);
-    q.idx = __shfl_xor_sync(0xffffffffu, p.idx, o);
-    q.bad = __shfl_xor_sync(0xffffffffu, p.bad, o);
-    return merge_p1<kSum>(p, q, c);
-}
-
-// One block reduction of pass 1's per-thread results: shuffle trees within
-// each warp, then warp 0 merges the warp results (fixed order).
+// The block result of pass 1 from each thread's (max, sum rescaled to it,
+// lowest index holding the max or INT_MAX, NaN seen).  Each warp takes its
+// max, rescales every lane's sum to it once and adds them in a fixed
+// float-float tree; warp 0 does the same over the warps.  Two barriers.
 template <bool kSum>
 __device__ __forceinline__ Pass1 reduce_pass1(float m, ff z, int idx, bool bad, float c, BlockScratch& s) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    P1Part p{m, z, idx, bad ? 1 : 0};
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) p = shfl_merge_p1<kSum>(p, o, c);
+    const float mw = warp_max(m);
+    idx = warp_min_i(m == mw ? idx : 0x7fffffff);
+    const int bw = __any_sync(0xffffffffu, bad) ? 1 : 0;
+    ff zw = ff{0.0f, 0.0f};
+    if (kSum) zw = warp_sum_ff((m > -INFINITY) ? ff_scale(z, ex2((m - mw) * c)) : ff{0.0f, 0.0f});
     if (lane == 0) {
-        s.pf[w] = p.m;
-        s.pf2[w] = p.z.hi;
-        s.pf3[w] = p.z.lo;
-        s.pi[w] = p.idx;
-        s.pi2[w] = p.bad;
+        s.pf[w] = mw;
+        s.pf2[w] = zw.hi;
+        s.pf3[w] = zw.lo;
+        s.pi[w] = idx;
+        s.pi2[w] = bw;
     }
     __syncthreads();
     if (w == 0) {
-        P1Part q = (lane < kNW) ? P1Part{s.pf[lane], ff{s.pf2[lane], s.pf3[lane]}, s.pi[lane], s.pi2[lane]}
-                                : P1Part{-INFINITY, ff{0.0f, 0.0f}, 0x7fffffff, 0};
-        __syncwarp();
-#pragma unroll
-        for (int o = kNW / 2; o > 0; o >>= 1) q = shfl_merge_p1<kSum>(q, o, c);
+        const float mi = (lane < kNW) ? s.pf[lane] : -INFINITY;
+        const float M = warp_max(mi);
+        const int I = warp_min_i((lane < kNW && mi == M) ? s.pi[lane] : 0x7fffffff);
+        const int Bd = __any_sync(0xffffffffu, lane < kNW && s.pi2[lane] != 0) ? 1 : 0;
+        ff Z = ff{0.0f, 0.0f};
+        if (kSum) {
+            const ff zi = (lane < kNW && mi > -INFINITY) ? ff_scale(ff{s.pf2[lane], s.pf3[lane]}, ex2((mi - M) * c))
+                                                          : ff{0.0f, 0.0f};
+            Z = warp_sum_ff(zi);
+        }
         if (lane == 0) {
-            s.rf[kNW] = q.m;
-            s.rf[kNW + 1] = q.z.hi;
-            s.rf2[kNW] = q.z.lo;
-            s.ri[kNW] = q.idx;
-            s.ri[kNW + 1] = q.bad;
+            s.rf[kNW] = M;
+            s.rf[kNW + 1] = Z.hi;
+            s.rf2[kNW] = Z.lo;
+            s.ri[kNW] = I;
+            s.ri[kNW + 1] = Bd;
         }
     }
     __syncthreads();
@@ -263,9 +240,12 @@ __device__ Pass1 row_pass1(const T* __restrict__ row, int V, float c, BlockScrat
         take_scalar(x_tail);
     }
 
-    // Lowest index of this thread holding m_t: head < body < tail.
+    // Lowest index of this thread holding m_t (head < body < tail), searched
+    // only by the lanes that hold their warp's max.
     int idx = 0x7fffffff;
-    if (tid < rv.head && x_head == m_t) {
+    const bool holds = (m_t == warp_max(m_t));
+    if (!holds) {
+    } else if (tid < rv.head && x_head == m_t) {
         idx = tid;
     } else if (best_batch >= 0 && best_bm == m_t) {
         for (int u = 0; u < kUnroll && idx == 0x7fffffff; ++u) {
