@@ -602,12 +602,10 @@ __device__ WalkOut walk_keys(const uint32_t* hist, int nbins, const WalkMap& map
 // Counts of the keys in [klo, khi] into hist[khi - key]; -0 is counted as
 // +0 when both are in the window.
 __device__ inline void count_key_window(const __nv_bfloat16* __restrict__ row, int V, int klo, int khi,
-                                        uint32_t* hist, BlockScratch& s) {
+                                        uint32_t* hist) {
     const RowView<__nv_bfloat16> rv(row, V);
     const int tid = threadIdx.x;
     const int nb = khi - klo + 1;
-    for (int i = tid; i < nb; i += kNT) hist[i] = 0u;
-    __syncthreads();
     auto take = [&](uint32_t b) {
         const uint32_t idx = (uint32_t)(khi - (int)okey16(b));
         if (idx < (uint32_t)nb) atomicAdd(&hist[idx], 1u);
@@ -638,22 +636,143 @@ __device__ inline void count_key_window(const __nv_bfloat16* __restrict__ row, i
         hist[khi - 0x8000] += hist[khi - 0x7fff];
         hist[khi - 0x7fff] = 0u;
     }
+}
+
+// Counts of the keys of a window on one side of zero: one predicated shared
+// reduction per element, at an address formed from the element's bits.
+// NEG = false (klo > +0): position key - klo, since a positive element's key
+// is its bits + 0x8000; NEG = true (khi < -0): position khi - key, since a
+// negative element's key is 0xffff - its bits.  TOP: khi is the row's
+// largest key, so no element lies above the window.  COPIES interleaved
+// copies of the histogram (hist[pos * COPIES + copy], the copy chosen by
+// lane / (32 / COPIES)) put lanes of different groups in different banks;
+// the caller sums them.
+template <bool NEG, bool TOP, int COPIES>
+__device__ inline void count_window_signed(const __nv_bfloat16* __restrict__ row, int V, int klo, int khi,
+                                           uint32_t* hist) {
+    static_assert(COPIES == 1 || COPIES == 2 || COPIES == 4 || COPIES == 8, "copies: a power of two up to 8");
+    constexpr int kLgC = COPIES == 8 ? 3 : (COPIES == 4 ? 2 : (COPIES == 2 ? 1 : 0));
+    const RowView<__nv_bfloat16> rv(row, V);
+    const int tid = threadIdx.x;
+    const float t_lo = key_value(klo), t_hi = key_value(khi);
+    const uint32_t copy = (uint32_t)(tid & 31) >> (5 - kLgC);
+    const uint32_t base = (uint32_t)__cvta_generic_to_shared(hist) + 4u * copy;
+    const uint32_t kb = NEG ? base - 4u * COPIES * (uint32_t)(0xffff - khi) : base - 4u * COPIES * (uint32_t)(klo - 0x8000);
+    auto take = [&](uint32_t xb) {  // xb: the element's float bit pattern (bf16 bits << 16)
+        const uint32_t addr = kb + (xb >> (14 - kLgC));
+        if (TOP) {
+            asm volatile("{\n\t.reg .pred p;\n\tsetp.ge.f32 p, %0, %1;\n\t@p red.shared.add.u32 [%2], 1;\n\t}"
+                         ::"f"(__uint_as_float(xb)), "f"(t_lo), "r"(addr)
+                         : "memory");
+        } else {
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tsetp.ge.f32 p, %0, %1;\n\tsetp.le.and.f32 p, %0, %3, p;\n\t"
+                "@p red.shared.add.u32 [%2], 1;\n\t}"
+                ::"f"(__uint_as_float(xb)), "f"(t_lo), "r"(addr), "f"(t_hi)
+                : "memory");
+        }
+    };
+    if (tid < rv.head) take((uint32_t)(*reinterpret_cast<const unsigned short*>(row + tid)) << 16);
+    const uint4* vp = rv.vec();
+    const uint64_t last_use = l2_evict_first_policy();
+    constexpr int kU2 = 4;
+    for (int base_v = tid; base_v < rv.nvec; base_v += kU2 * kNT) {
+        uint4 v[kU2];
+#pragma unroll
+        for (int u = 0; u < kU2; ++u) {
+            const int vi = base_v + u * kNT;
+            v[u] = (vi < rv.nvec) ? ldg_last_use(vp + vi, last_use) : neg_inf_vec<__nv_bfloat16>();
+        }
+#pragma unroll
+        for (int u = 0; u < kU2; ++u) {
+            const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                take(w4[j] << 16);
+                take(w4[j] & 0xffff0000u);
+            }
+        }
+    }
+    if (tid < rv.tail)
+        take((uint32_t)(*reinterpret_cast<const unsigned short*>(row + rv.head + rv.nvec * 8 + tid)) << 16);
+}
+
+// Sums the 8 interleaved copies of an nb-position histogram (nb <= 4 * kNT)
+// into hist[0, nb).
+__device__ inline void merge_copies8(uint32_t* hist, int nb) {
+    uint32_t sum[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = threadIdx.x + j * kNT;
+        sum[j] = 0u;
+        if (i < nb) {
+            const uint4 a = reinterpret_cast<const uint4*>(hist)[2 * i];
+            const uint4 b = reinterpret_cast<const uint4*>(hist)[2 * i + 1];
+            sum[j] = (a.x + a.y) + (a.z + a.w) + (b.x + b.y) + (b.z + b.w);
+        }
+    }
     __syncthreads();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int i = threadIdx.x + j * kNT;
+        if (i < nb) hist[i] = sum[j];
+    }
+}
+
+// One-signed window count, interleaved 8 ways when the window is narrow.
+template <bool NEG>
+__device__ inline void count_window_one_sign(const __nv_bfloat16* __restrict__ row, int V, int klo, int khi,
+                                             bool top, uint32_t* hist) {
+    const int nb = khi - klo + 1;
+    if (nb <= 4 * kNT && 8 * nb <= kFullBins) {
+        for (int i = threadIdx.x; i < 8 * nb; i += kNT) hist[i] = 0u;
+        __syncthreads();
+        if (top) count_window_signed<NEG, true, 8>(row, V, klo, khi, hist);
+        else count_window_signed<NEG, false, 8>(row, V, klo, khi, hist);
+        __syncthreads();
+        merge_copies8(hist, nb);
+    } else {
+        for (int i = threadIdx.x; i < nb; i += kNT) hist[i] = 0u;
+        __syncthreads();
+        if (top) count_window_signed<NEG, true, 1>(row, V, klo, khi, hist);
+        else count_window_signed<NEG, false, 1>(row, V, klo, khi, hist);
+    }
 }
 
 // Exact nucleus by counting key windows from key_top down to key_floor,
 // starting at mass F0 above key_top.  Each window is one pass over the row
-// (from L2) and one walk.
+// (from L2) and one walk.  The first window stops at first_lo when that is
+// higher; top: key_top is the row's largest key.
 __device__ inline Topp topp_windows(const __nv_bfloat16* __restrict__ row, int V, float c, float mc, ff Z, ff pZ,
-                                    int key_top, int key_floor, ff F0, uint32_t* hist, BlockScratch& s) {
+                                    int key_top, int key_floor, ff F0, uint32_t* hist, BlockScratch& s,
+                                    int first_lo = 0, bool top = false) {
     if (key_floor == 0x8000) key_floor = 0x7fff;  // -0 belongs with +0
     for (int hi = key_top; hi >= key_floor;) {
         int lo = hi - kFullBins + 1;
         if (lo < key_floor) lo = key_floor;
+        if (hi == key_top && lo < first_lo) lo = first_lo;
         if (lo == 0x8000 && hi > 0x8000) lo = 0x8001;  // keep +0 and -0 in one window
-        count_key_window(row, V, lo, hi, hist, s);
+        const int nb = hi - lo + 1;
+        const bool pos = lo > 0x8000, neg = hi < 0x7fff, at_top = top && hi == key_top;
+        if (pos) {
+            count_window_one_sign<false>(row, V, lo, hi, at_top, hist);
+        } else if (neg) {
+            count_window_one_sign<true>(row, V, lo, hi, at_top, hist);
+        } else {
+            for (int i = threadIdx.x; i < nb; i += kNT) hist[i] = 0u;
+            __syncthreads();
+            count_key_window(row, V, lo, hi, hist);
+        }
+        __syncthreads();
         ff F_end;
-        const WalkOut o = walk_keys<false>(hist, hi - lo + 1, plain_map(hi), c, mc, F0, pZ, &F_end, s);
+        WalkOut o;
+        if (pos) {
+            o = (nb <= 2048) ? walk_keys<true, true>(hist, nb, plain_map(hi), c, mc, F0, pZ, &F_end, s)
+                             : walk_keys<false, true>(hist, nb, plain_map(hi), c, mc, F0, pZ, &F_end, s);
+        } else {
+            o = (nb <= 2048) ? walk_keys<true, false>(hist, nb, plain_map(hi), c, mc, F0, pZ, &F_end, s)
+                             : walk_keys<false, false>(hist, nb, plain_map(hi), c, mc, F0, pZ, &F_end, s);
+        }
         if (o.found == 1) return o.r;
         F0 = F_end;
         hi = lo - 1;
@@ -1032,8 +1151,11 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
         }
         __syncthreads();  // the estimate's shared memory becomes the histogram
     }
-    if (route == 1) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_a, ff{0.0f, 0.0f}, hist, s);
-    if (route == 0) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_lo, ff{0.0f, 0.0f}, hist, s);
+    if (route == 1) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_a, ff{0.0f, 0.0f}, hist, s, 0, true);
+    if (route == 0) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_lo, ff{0.0f, 0.0f}, hist, s, 0, true);
+    // A bracket above zero: counting every key from t_a up to the max costs
+    // less per element than weighing the elements above t_b.
+    if (key_a > 0x8000) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_lo, ff{0.0f, 0.0f}, hist, s, key_a, true);
 
     const bool spans = key_a <= 0x8000 && key_b >= 0x8000;
     const MixedLayout L(key_a, key_b);
@@ -1041,23 +1163,16 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
     for (int i = tid; i < W; i += kNT) hist[i] = 0u;
     __syncthreads();
     ff part, lpart = ff{0.0f, 0.0f};
-    if (key_a > 0x8000) part = band_pass<0>(row, V, c, mc, key_a, key_b, hist);
-    else if (!spans) part = band_pass<1>(row, V, c, mc, key_a, key_b, hist);
+    if (!spans) part = band_pass<1>(row, V, c, mc, key_a, key_b, hist);
     else band_pass_mixed(row, V, c, mc, L, hist, part, lpart);
     const ff F_above = block_sum_ff(part, s);  // its barriers also publish the counts
     const ff lump = spans ? block_sum_ff(lpart, s) : ff{0.0f, 0.0f};
     if (ff_ge(F_above, pZ))  // the boundary lies above the bracket
         return topp_windows(row, V, c, mc, Z, pZ, kmax, key_b + 1, ff{0.0f, 0.0f}, hist, s);
     ff F_end;
-    WalkOut o;
-    if (key_a > 0x8000) {
-        o = (W <= 2048) ? walk_keys<true, true>(hist, W, plain_map(key_b), c, mc, F_above, pZ, &F_end, s)
-                        : walk_keys<false, true>(hist, W, plain_map(key_b), c, mc, F_above, pZ, &F_end, s);
-    } else {
-        const WalkMap map = spans ? WalkMap{key_b, L.Wp, L.kn_top, lump} : plain_map(key_b);
-        o = (W <= 2048) ? walk_keys<true, false>(hist, W, map, c, mc, F_above, pZ, &F_end, s)
-                        : walk_keys<false, false>(hist, W, map, c, mc, F_above, pZ, &F_end, s);
-    }
+    const WalkMap map = spans ? WalkMap{key_b, L.Wp, L.kn_top, lump} : plain_map(key_b);
+    const WalkOut o = (W <= 2048) ? walk_keys<true, false>(hist, W, map, c, mc, F_above, pZ, &F_end, s)
+                                  : walk_keys<false, false>(hist, W, map, c, mc, F_above, pZ, &F_end, s);
     if (o.found == 1) return o.r;
     if (o.found == 2) {  // inside the lump: count its keys exactly, from the mass above it
         const int top = key_b < kLumpPosKey - 1 ? key_b : kLumpPosKey - 1;
