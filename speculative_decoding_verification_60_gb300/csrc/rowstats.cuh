@@ -675,7 +675,7 @@ __device__ inline void count_window_signed(const __nv_bfloat16* __restrict__ row
     if (tid < rv.head) take((uint32_t)(*reinterpret_cast<const unsigned short*>(row + tid)) << 16);
     const uint4* vp = rv.vec();
     const uint64_t last_use = l2_evict_first_policy();
-    constexpr int kU2 = 4;
+    constexpr int kU2 = 8;  // L2 (partly DRAM) re-read: 8 vectors in flight per thread
     for (int base_v = tid; base_v < rv.nvec; base_v += kU2 * kNT) {
         uint4 v[kU2];
 #pragma unroll
@@ -766,8 +766,8 @@ __device__ inline Topp topp_windows(const __nv_bfloat16* __restrict__ row, int V
         __syncthreads();
         ff F_end;
         WalkOut o;
-        if (pos) {
-            o = (nb <= 2048) ? walk_keys<true, true>(hist, nb, plain_map(hi), c, mc, F0, pZ, &F_end, s)
+        if (pos) {  // warp 0 alone walks short windows; the block walks longer ones
+            o = (nb <= 256) ? walk_keys<true, true>(hist, nb, plain_map(hi), c, mc, F0, pZ, &F_end, s)
                              : walk_keys<false, true>(hist, nb, plain_map(hi), c, mc, F0, pZ, &F_end, s);
         } else {
             o = (nb <= 2048) ? walk_keys<true, false>(hist, nb, plain_map(hi), c, mc, F0, pZ, &F_end, s)
