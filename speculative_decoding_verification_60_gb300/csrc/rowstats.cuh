@@ -791,22 +791,19 @@ __device__ __forceinline__ float warp_sum_f(float v) {
     return v;
 }
 
-// Second pass of the bracketed route, one read of the row (from L2): the
+// Second pass of a bracket below -0, one read of the row (from L2): the
 // exact mass of the elements above t_b (returned as this thread's part) and
-// the exact counts of the keys in [t_a, t_b].  SGN 0: the bracket lies above
-// +0, counts in hist[key - key_a]; 1: below -0, hist[key_b - key].  A count
+// the exact counts of the keys in [t_a, t_b], in hist[key_b - key].  A count
 // is addressed by one add to the element's float bit pattern shifted right
-// by 14 (4 * its bf16 bits).
-template <int SGN>
-__device__ ff band_pass(const __nv_bfloat16* __restrict__ row, int V, float c, float mc, int key_a, int key_b,
-                        uint32_t* hist) {
+// by 14 (4 * its bf16 bits), since a negative element's key is 0xffff - its
+// bits.
+__device__ ff band_pass_neg(const __nv_bfloat16* __restrict__ row, int V, float c, float mc, int key_a, int key_b,
+                            uint32_t* hist) {
     const RowView<__nv_bfloat16> rv(row, V);
     const int tid = threadIdx.x;
     const float t_a = key_value(key_a), t_b = key_value(key_b);
     const uint32_t base = (uint32_t)__cvta_generic_to_shared(hist);
-    const uint32_t k0 = base - 4u * (uint32_t)(key_a - 0x8000);  // SGN 0: k0 + 4 * bits
-    const uint32_t k1 = base - 4u * (uint32_t)(0xffff - key_b);  // SGN 1: k1 + 4 * bits
-    const uint32_t kb = (SGN == 0) ? k0 : k1;
+    const uint32_t kb = base - 4u * (uint32_t)(0xffff - key_b);
     // One element, branch-free: returns x's exponent argument when x is above
     // t_b (-inf otherwise) and counts x when it lies inside [t_a, t_b]; xb is
     // x's float bit pattern (bf16 bits << 16).
@@ -956,9 +953,11 @@ __device__ inline void band_pass_mixed(const __nv_bfloat16* __restrict__ row, in
 //       and the sample estimates its mass with a computable standard error:
 //       the bracket [t_a, t_b] is where the estimated tail mass crosses
 //       (1 - top_p) * Z widened by four standard errors and one bin.
-//  2. One pass from L2: exact mass above t_b, exact key counts inside.
-//  3. Walk the bracket.  When the boundary is outside it, the exact counted
-//     windows take over from the side it lies on.
+//  2. One pass from L2.  A bracket above zero: exact counts of every key
+//     from t_a up to the max (the walk then starts at the max).  Otherwise:
+//     exact mass above t_b and exact key counts inside the bracket.
+//  3. Walk the key counts.  When the boundary is outside the bracket, the
+//     exact counted windows take over from the side it lies on.
 // smem: kTopSmemBytes holding the pass-1 sample and thread maxima.
 __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int V, float c, float m, ff Z,
                                      float top_p, uint8_t* smem, BlockScratch& s) {
@@ -1163,7 +1162,7 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
     for (int i = tid; i < W; i += kNT) hist[i] = 0u;
     __syncthreads();
     ff part, lpart = ff{0.0f, 0.0f};
-    if (!spans) part = band_pass<1>(row, V, c, mc, key_a, key_b, hist);
+    if (!spans) part = band_pass_neg(row, V, c, mc, key_a, key_b, hist);
     else band_pass_mixed(row, V, c, mc, L, hist, part, lpart);
     const ff F_above = block_sum_ff(part, s);  // its barriers also publish the counts
     const ff lump = spans ? block_sum_ff(lpart, s) : ff{0.0f, 0.0f};
