@@ -59,7 +59,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         for out in ex.map(run, jobs):
             if verbose and out.strip():
                 print(out)
-    if force or jobs or not os.path.exists(LIB):
+    # relink also when an earlier link failed after its objects were built
+    if force or jobs or not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
         tmp = LIB + f".{os.getpid()}.tmp"
         run([nvcc, *ARCH, "-shared", "-o", tmp, *objs])
         os.replace(tmp, LIB)

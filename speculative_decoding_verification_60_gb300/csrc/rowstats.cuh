@@ -797,7 +797,7 @@ __device__ __forceinline__ float warp_sum_f(float v) {
 // is addressed by one add to the element's float bit pattern shifted right
 // by 14 (4 * its bf16 bits), since a negative element's key is 0xffff - its
 // bits.
-__device__ ff band_pass_neg(const __nv_bfloat16* __restrict__ row, int V, float c, float mc, int key_a, int key_b,
+__device__ inline ff band_pass_neg(const __nv_bfloat16* __restrict__ row, int V, float c, float mc, int key_a, int key_b,
                             uint32_t* hist) {
     const RowView<__nv_bfloat16> rv(row, V);
     const int tid = threadIdx.x;
