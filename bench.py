@@ -92,13 +92,24 @@ def job_value(rows_per_rank: int, world: int, ms: float) -> float:
 
 
 def source_sha() -> str:
-    """Hash of the kernel sources, to tell whether recorded counters still apply."""
-    h = hashlib.sha256()
+    """Hash of the row-statistics kernel's sources (linear.cu and every
+    kernel header it includes, transitively), to tell whether recorded
+    counters still apply."""
     csrc = os.path.join(ROOT, "speculative_decoding_verification_60_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(f.encode())
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    seen, todo = set(), ["linear.cu"]
+    while todo:
+        f = todo.pop()
+        if f in seen or not os.path.exists(os.path.join(csrc, f)):
+            continue
+        seen.add(f)
+        for line in open(os.path.join(csrc, f)):
+            line = line.strip()
+            if line.startswith("#include \"") and "/" not in line:
+                todo.append(line.split('"')[1])
+    h = hashlib.sha256()
+    for f in sorted(seen):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -375,6 +386,38 @@ def time_e2e(step: LinearStep, K: int, chunks: int = 4):
     return e0.elapsed_time(e1) / K, h2d, d2h, chunks
 
 
+def time_sampler(step: LinearStep, K: int, W: int, peak: float):
+    """Draft-side sampling (spec_sample_rows) of one token per request: the
+    first B draft rows of the batch, V = 128256 bf16, the workload's T and
+    top-p.  The 64 MB of rows fit in L2, so L2 is flushed (a 256 MB write)
+    before every timed launch, each launch timed alone with CUDA events."""
+    torch = step.torch
+    B, V = step.B, step.V
+    rows = step.drf.reshape(-1, V)[:B]
+    req = torch.arange(B, dtype=torch.int64, device=step.dev)
+    pos = torch.full((B,), 1001, dtype=torch.int64, device=step.dev)
+    out = dict(out_tokens=torch.empty(B, dtype=torch.int32, device=step.dev),
+               dev_error=torch.empty(1, dtype=torch.int32, device=step.dev))
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=step.dev)
+    s = torch.cuda.current_stream()
+    for _ in range(W):
+        step.svp.sample_rows(rows, step.T, step.top_p, step.seed, req, pos, out=out, stream=s)
+    ts = []
+    for _ in range(K):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        step.svp.sample_rows(rows, step.T, step.top_p, step.seed, req, pos, out=out, stream=s)
+        e1.record(s)
+        e1.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = statistics.mean(ts)
+    gbps = B * V * 2 / (ms / 1e3) / 1e9
+    return {"workload": f"{B} rows of V={V} bf16, T={step.T}, top-p {step.top_p}", "ms": round(ms, 4),
+            "rows_per_s": round(B / (ms / 1e3), 1), "gbps": round(gbps, 1), "frac": round(gbps / peak, 4),
+            "launches": K, "l2": "flushed before every launch"}
+
+
 def time_tree(device, K: int, W: int):
     import numpy as np
     import torch
@@ -459,6 +502,8 @@ def run_ours(args):
     e2e_ms, h2d, d2h, chunks = (ms, 0, 0, 1) if args.no_e2e else time_e2e(step, args.e2e_steps)
     e2e_ms = max_over_ranks([e2e_ms], world, device)[0]
     tree = None if args.no_tree else time_tree(device, max(3, args.steps // 2), 2)
+    peak0, _ = hbm_peak()
+    sampler = time_sampler(step, max(3, min(50, args.steps)), 3, peak0)
     peak, peak_kind = hbm_peak()
     achieved = step.algo_bytes / (stats_ms / 1e3) / 1e9
     acc = step.acc.cpu()
@@ -490,6 +535,7 @@ def run_ours(args):
         "clocks": clk,
         "mean_accepted_len": round(float(acc.float().mean()), 4),
         "tree": tree,
+        "draft_sampler": sampler,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(step, args.cpu_requests)

@@ -263,6 +263,36 @@ spec_status spec_compact_accepted(const void* hidden, int B, int T, int H, const
                                   int32_t* offsets, int32_t* next_tokens, int32_t* dev_error,
                                   spec_stream_t stream);
 
+/*
+ * Draft-side sampling: one token per logit row drawn from
+ * filter(softmax(row / T)), the draft model's own sampling of its tokens
+ * (section "Target-Draft"), done on the GPU so that a token drawn from
+ * logits carried over from the previous step reaches the next draft run
+ * without a host round trip (section "MTP schedule for a single token").
+ *
+ *  logits       [R, V] bf16 or fp32, row-major.
+ *  request_ids  [R] int64 or NULL (NULL => r); positions [R] int64 or NULL
+ *               (NULL => 0).  Row r draws u = Philox(seed, request_ids[r],
+ *               positions[r], purpose 4 = DRAFT, round 0) and returns the
+ *               smallest v with C(v) > u * C(V-1), C the running sum of the
+ *               filtered probabilities in index order (the filter as in
+ *               spec_verify_linear: temperature, then the exact top-p
+ *               nucleus with ties at the boundary kept in index order).
+ *  out_tokens   [R] int32 out.
+ *  params       temperature == 0: the lowest-index maximum over entries
+ *               that are neither NaN nor +inf (0 when there is none), with
+ *               no error.  temperature > 0: a row holding a NaN or +inf, or
+ *               no finite entry, sets SPEC_DEVERR_NONFINITE and yields that
+ *               argmax.  child_mode is ignored.
+ *  dev_error    [1] or NULL.
+ *  Errors: SPEC_ERR_INVALID_ARG (NULL logits / out_tokens / params, R < 1,
+ *  V < 1, temperature < 0 or not finite, top_p <= 0 or NaN, dtype not
+ *  bf16 or fp32); SPEC_ERR_UNSUPPORTED (V above 524,280).
+ */
+spec_status spec_sample_rows(const void* logits, spec_dtype dtype, int R, int V, const int64_t* request_ids,
+                             const int64_t* positions, const spec_sampling_params* params, int32_t* out_tokens,
+                             int32_t* dev_error, spec_stream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* spec_status_string(spec_status status);
 

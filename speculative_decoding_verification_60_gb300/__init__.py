@@ -21,6 +21,7 @@ from ._binding import (  # noqa: F401
     SpecError,
     compact_accepted,
     load,
+    sample_rows,
     status_string,
     verify_linear,
     verify_tree,

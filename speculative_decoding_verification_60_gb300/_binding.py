@@ -24,7 +24,8 @@ DEVERR_TOKEN, DEVERR_NONFINITE, DEVERR_PARENT, DEVERR_LENGTH = 1, 2, 4, 8
 
 # Every symbol declared in include/specverify.h.
 EXPORTS = ("spec_workspace_size", "spec_verify_linear", "spec_linear_stats", "spec_linear_decide",
-           "spec_verify_linear_noalloc", "spec_verify_tree", "spec_compact_accepted", "spec_status_string")
+           "spec_verify_linear_noalloc", "spec_verify_tree", "spec_compact_accepted", "spec_sample_rows",
+           "spec_status_string")
 
 
 class SamplingParams(ctypes.Structure):
@@ -69,6 +70,8 @@ def load() -> ctypes.CDLL:
     lib.spec_verify_tree.restype = I
     lib.spec_compact_accepted.argtypes = [P, I, I, I, P, P, P, I, P, P, P, P, P]
     lib.spec_compact_accepted.restype = I
+    lib.spec_sample_rows.argtypes = [P, I, I, I, P, P, ctypes.POINTER(SamplingParams), P, P, P]
+    lib.spec_sample_rows.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -217,4 +220,28 @@ def compact_accepted(hidden, accepted_len, out_tokens, path_nodes=None, stream=N
                                    _ptr(out["dev_error"]), _stream(stream))
     if st != SPEC_OK:
         raise SpecError("spec_compact_accepted", st)
+    return out
+
+
+def sample_rows(logits, temperature: float, top_p: float = 1.0, seed: int = 0, request_ids=None, positions=None,
+                out=None, stream=None) -> dict:
+    """``spec_sample_rows`` on torch tensors: one token per row of logits
+    [R, V] (bf16 or fp32) from filter(softmax(row / temperature)).
+    request_ids and positions [R] int64 or None.  Returns a dict of device
+    tensors: out_tokens [R] int32, dev_error [1] int32."""
+    lib = load()
+    R, V = logits.shape
+    dt = _dtype_code(logits)
+    _check(logits, "logits")
+    _check(request_ids, "request_ids", torch.int64, (R,))
+    _check(positions, "positions", torch.int64, (R,))
+    dev = logits.device
+    if out is None:
+        out = dict(out_tokens=torch.empty(R, dtype=torch.int32, device=dev),
+                   dev_error=torch.empty(1, dtype=torch.int32, device=dev))
+    sp = SamplingParams(float(temperature), float(top_p), int(seed) & (2**64 - 1), 0)
+    st = lib.spec_sample_rows(_ptr(logits), dt, R, V, _ptr(request_ids), _ptr(positions), ctypes.byref(sp),
+                              _ptr(out["out_tokens"]), _ptr(out.get("dev_error")), _stream(stream))
+    if st != SPEC_OK:
+        raise SpecError("spec_sample_rows", st)
     return out

@@ -82,6 +82,25 @@ def test_host_argument_checks_return_status(lib):
     assert lib.spec_compact_accepted(None, 1, 1, 8, dummy, None, dummy, 1, dummy, dummy, dummy, None, None) == 1
 
 
+def test_sample_rows_host_checks(lib):
+    """spec_sample_rows rejects bad calls before any CUDA call."""
+    from speculative_decoding_verification_60_gb300 import SamplingParams
+
+    sp = SamplingParams(0.7, 0.9, 0, 0)
+    dummy = ctypes.c_void_p(16)
+    call = lambda logits, dt, R, V, p, out: lib.spec_sample_rows(logits, dt, R, V, None, None, p, out, None, None)
+    assert call(None, 0, 1, 8, ctypes.byref(sp), dummy) == 1  # no logits
+    assert call(dummy, 0, 1, 8, None, dummy) == 1  # no params
+    assert call(dummy, 0, 1, 8, ctypes.byref(sp), None) == 1  # no output
+    assert call(dummy, 7, 1, 8, ctypes.byref(sp), dummy) == 1  # unknown dtype
+    assert call(dummy, 0, 0, 8, ctypes.byref(sp), dummy) == 1  # R < 1
+    assert call(dummy, 0, 1, 0, ctypes.byref(sp), dummy) == 1  # V < 1
+    for T, p in ((-1.0, 0.9), (float("inf"), 0.9), (float("nan"), 0.9), (0.7, 0.0), (0.7, float("nan"))):
+        bad = SamplingParams(T, p, 0, 0)
+        assert call(dummy, 0, 1, 8, ctypes.byref(bad), dummy) == 1, (T, p)
+    assert call(dummy, 0, 1, 524281, ctypes.byref(sp), dummy) == 2  # V above the limit
+
+
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import speculative_decoding_verification_60_gb300._binding as b
 
