@@ -108,3 +108,17 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not found"):
         b.load()
+
+
+def test_sample_rows_binding_checks(lib):
+    """The Python binding refuses what the C call cannot take before calling it."""
+    import torch
+
+    import speculative_decoding_verification_60_gb300 as svp
+
+    with pytest.raises(ValueError, match="CUDA"):
+        svp.sample_rows(torch.zeros(2, 8, dtype=torch.bfloat16), 0.7, 0.9)  # host tensor
+    with pytest.raises(TypeError, match="bfloat16 or float32"):
+        svp.sample_rows(torch.zeros(2, 8, dtype=torch.float16), 0.7, 0.9)
+    with pytest.raises(ValueError):
+        svp.sample_rows(torch.zeros(2, 3, 8, dtype=torch.bfloat16), 0.7, 0.9)  # not [R, V]
