@@ -84,6 +84,8 @@ typedef enum { SPEC_OP_LINEAR = 0, SPEC_OP_TREE = 1 } spec_op;
 #define SPEC_DEVERR_NONFINITE 2  /* NaN or +inf logit, or no finite logit in a row */
 #define SPEC_DEVERR_PARENT 4     /* parent[] not a tree rooted at 0 with parent[i] < i, or deeper than max_depth */
 #define SPEC_DEVERR_LENGTH 8     /* compaction: accepted length or source row out of range */
+#define SPEC_DEVERR_TIMEOUT 16   /* a wait for a bulk copy ran out (2 s); the rows it left were
+                                    recomputed by the two-pass route, so the results stand */
 
 typedef struct {
     float temperature;  /* 0 => greedy (argmax, ties to the lowest index); > 0 => sampled */

@@ -28,6 +28,7 @@ constexpr int kDevErrToken = 1;
 constexpr int kDevErrNonfinite = 2;
 constexpr int kDevErrParent = 4;
 constexpr int kDevErrLength = 8;
+constexpr int kDevErrTimeout = 16;
 
 // ---------------------------------------------------------------- Philox --
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as
@@ -111,6 +112,33 @@ __device__ __forceinline__ uint32_t bf16_bits_round_down(float f) {
     const uint32_t t = b >> 16;
     if ((b & 0xffffu) == 0u) return t;
     return (b & 0x80000000u) ? t + 1u : t;  // negative: more negative is larger magnitude
+}
+
+// ------------------------------------------------------------- barriers --
+// Barrier over the kNT threads that work on a row.  A unit whose CTAs hold
+// other warps beside them (a warp issuing bulk copies) defines
+// SV_ROW_BARRIER_NAMED, so that these barriers count the kNT row threads
+// only (named barrier 1); elsewhere they are the CTA barrier.
+__device__ __forceinline__ void row_sync() {
+#ifdef SV_ROW_BARRIER_NAMED
+    asm volatile("bar.sync 1, %0;" ::"n"(kNT) : "memory");
+#else
+    __syncthreads();
+#endif
+}
+// row_sync that also returns whether v was true in any row thread.
+__device__ __forceinline__ bool row_sync_or(bool v) {
+#ifdef SV_ROW_BARRIER_NAMED
+    uint32_t r;
+    asm volatile("{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, %2, p;\n\t"
+                 "selp.u32 %0, 1, 0, q;\n\t}"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "n"(kNT)
+                 : "memory");
+    return r != 0;
+#else
+    return __syncthreads_or(v ? 1 : 0) != 0;
+#endif
 }
 
 // ------------------------------------------------------- block reductions --
@@ -224,57 +252,57 @@ __device__ __forceinline__ int warp_inclusive_scan_i(int x) {
     return x;
 }
 
-// All threads of the CTA must call these.
+// All kNT row threads must call these.
 __device__ __forceinline__ float block_max(float v, BlockScratch& s) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_max(v);
     if (lane == 0) s.pf[w] = v;
-    __syncthreads();
+    row_sync();
     if (w == 0) {
         float r = warp_max(lane < kNW ? s.pf[lane] : -INFINITY);
         if (lane == 0) s.rf[0] = r;
     }
-    __syncthreads();
+    row_sync();
     return s.rf[0];
 }
 __device__ __forceinline__ int block_min_i(int v, BlockScratch& s) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_min_i(v);
     if (lane == 0) s.pi[w] = v;
-    __syncthreads();
+    row_sync();
     if (w == 0) {
         const int r = warp_min_i(lane < kNW ? s.pi[lane] : 0x7fffffff);
         if (lane == 0) s.ri[0] = r;
     }
-    __syncthreads();
+    row_sync();
     return s.ri[0];
 }
 __device__ __forceinline__ int block_sum_i(int v, BlockScratch& s) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_sum_i(v);
     if (lane == 0) s.pi[w] = v;
-    __syncthreads();
+    row_sync();
     if (w == 0) {
         const int r = warp_sum_i(lane < kNW ? s.pi[lane] : 0);
         if (lane == 0) s.ri[0] = r;
     }
-    __syncthreads();
+    row_sync();
     return s.ri[0];
 }
 __device__ __forceinline__ bool block_any(bool v, BlockScratch& s) {
-    return __syncthreads_or(v ? 1 : 0) != 0;
+    return row_sync_or(v);
 }
 // Deterministic block sum in float-float: fixed shuffle trees.
 __device__ __forceinline__ ff block_sum_ff(ff v, BlockScratch& s) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     v = warp_sum_ff(v);
     if (lane == 0) { s.pf[w] = v.hi; s.pf2[w] = v.lo; }
-    __syncthreads();
+    row_sync();
     if (w == 0) {
         const ff r = warp_sum_ff(lane < kNW ? ff{s.pf[lane], s.pf2[lane]} : ff{0.0f, 0.0f});
         if (lane == 0) { s.rf[0] = r.hi; s.rf2[0] = r.lo; }
     }
-    __syncthreads();
+    row_sync();
     return ff{s.rf[0], s.rf2[0]};
 }
 // Exclusive prefix in thread order (float-float); *total receives the sum.
@@ -282,7 +310,7 @@ __device__ __forceinline__ ff block_exclusive_scan_ff(ff v, BlockScratch& s, ff*
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const ff x = warp_inclusive_scan_ff(v);
     if (lane == 31) { s.pf[w] = x.hi; s.pf2[w] = x.lo; }
-    __syncthreads();
+    row_sync();
     if (w == 0) {
         const ff t = (lane < kNW) ? ff{s.pf[lane], s.pf2[lane]} : ff{0.0f, 0.0f};
         const ff incl = warp_inclusive_scan_ff(t);
@@ -293,7 +321,7 @@ __device__ __forceinline__ ff block_exclusive_scan_ff(ff v, BlockScratch& s, ff*
         }
         if (lane == kNW - 1) { s.rf[kNW] = incl.hi; s.rf2[kNW] = incl.lo; }
     }
-    __syncthreads();
+    row_sync();
     if (total) *total = ff{s.rf[kNW], s.rf2[kNW]};
     return ff_add(ff{s.rf[w], s.rf2[w]}, ff_sub(x, v));
 }
@@ -301,14 +329,14 @@ __device__ __forceinline__ int block_exclusive_scan_i(int v, BlockScratch& s, in
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int x = warp_inclusive_scan_i(v);
     if (lane == 31) s.pi[w] = x;
-    __syncthreads();
+    row_sync();
     if (w == 0) {
         const int t = (lane < kNW) ? s.pi[lane] : 0;
         const int incl = warp_inclusive_scan_i(t);
         if (lane < kNW) s.ri[lane] = incl - t;
         if (lane == kNW - 1) s.ri[kNW] = incl;
     }
-    __syncthreads();
+    row_sync();
     if (total) *total = s.ri[kNW];
     return s.ri[w] + x - v;
 }
@@ -392,10 +420,13 @@ struct RowStat {
     float tau;     // top-p boundary logit; -inf when top-p is off
     int n_keep;    // boundary-valued tokens kept (the lowest-index ones)
     int c_tau;     // boundary-valued tokens in the row
-    int flags;     // kRowInvalid | kRowTokMember
+    int flags;     // kRowInvalid | kRowTokMember | kRowRedo
 };
 constexpr int kRowInvalid = 1;
 constexpr int kRowTokMember = 2;
+// Set by the one-read top-p pass on a row it leaves to the two-pass route
+// (the record's other fields are then undefined).
+constexpr int kRowRedo = 4;
 
 // Filtered probability of a logit x given the row's statistics; `rank_ok`
 // tells whether a boundary-valued token is among the kept ones.

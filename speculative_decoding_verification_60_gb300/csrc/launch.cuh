@@ -32,6 +32,11 @@ inline bool launch_grid(K kernel, size_t dyn_smem, long long work, int* grid, in
     if (dyn_smem > 0 &&
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) != cudaSuccess)
         return false;
+    // large shared-memory users ask for the whole carve-out, so that the
+    // resident-CTA count below is what runs
+    if (dyn_smem >= 48 * 1024 &&
+        cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+        return false;
     int per_sm = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, dyn_smem) != cudaSuccess) return false;
     const int sms = sm_count();

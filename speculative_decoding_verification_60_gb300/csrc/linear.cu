@@ -13,8 +13,9 @@
 namespace sv {
 
 // One CTA per row (persistent).  MODE 0 greedy, 1 sampled, 2 sampled + top-p.
+// redo_only: take only the rows the one-read top-p kernel marked kRowRedo.
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a) {
+__global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a, int redo_only) {
     extern __shared__ uint4 dyn_smem[];
     __shared__ BlockScratch s;
     __shared__ SampleScratch ss;
@@ -24,6 +25,7 @@ __global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a) {
     const T* tgt = static_cast<const T*>(a.tgt);
     const T* drf = static_cast<const T*>(a.drf);
     for (int r = blockIdx.x; r < R; r += gridDim.x) {
+        if (redo_only && !(a.stats[r].flags & kRowRedo)) continue;  // the same value in every thread
         const T* row;
         int tok;
         if (r < nt) {
@@ -42,15 +44,22 @@ __global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a) {
 }
 
 // Stage 1: statistics of every target and draft row into the workspace.
+// bf16 rows under top-p take the one-read kernel (rows_topp.cu) first; the
+// two-pass kernel then takes only the rows it left.
 template <typename T, int MODE>
 static spec_status launch_stats(LinearArgs& a, cudaStream_t st) {
     const int nt = a.B * (a.k + 1);
     const int R = nt + (MODE > 0 ? a.B * a.k : 0);
-    const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kTopSmemBytes : 0;
+    constexpr bool kOnePass = (MODE == 2 && sizeof(T) == 2);
+    if (kOnePass) {
+        const spec_status r = launch_rows_topp_onepass(a, st);
+        if (r != SPEC_OK) return r;
+    }
+    const size_t dyn = kOnePass ? (size_t)kTopSmemBytes : 0;
     auto* k1 = k_linear_rowstats<T, MODE>;
     int grid = 0;
     if (!launch_grid(k1, dyn, R, &grid, kNT)) return SPEC_ERR_CUDA;
-    k1<<<grid, kNT, dyn, st>>>(a);
+    k1<<<grid, kNT, dyn, st>>>(a, kOnePass ? 1 : 0);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -29,6 +29,10 @@ struct LinearArgs {
 __device__ __forceinline__ int tgt_row(const LinearArgs& a, int b, int i) { return b * (a.k + 1) + i; }
 __device__ __forceinline__ int drf_row(const LinearArgs& a, int b, int i) { return a.B * (a.k + 1) + b * a.k + i; }
 
+// Stage 1 for bf16 rows under top-p (rows_topp.cu): one read per row; rows
+// it cannot finish are marked kRowRedo for the two-pass kernel.
+spec_status launch_rows_topp_onepass(LinearArgs& a, cudaStream_t st);
+
 // Stage 2 (decide.cu): accept tests, accepted length and the residual or
 // bonus draw, one CTA per request.
 spec_status launch_decide_stage(LinearArgs& a, spec_dtype dtype, int mode, cudaStream_t st);

@@ -1,0 +1,343 @@
+// Row statistics of bf16 rows under top-p with one read of each row.
+//
+// "Accelerating Sonar through speculation", §Target-Draft: acceptance
+// compares the full probability distributions of draft and target, so each
+// row needs its normaliser and, with top-p filtering (applied to p and q
+// alike), its exact nucleus.
+//
+// Each CTA runs its rows on kNT row threads plus one copy warp.  The copy
+// warp streams every row through a ring of shared-memory slots with bulk
+// copies (cp.async.bulk, completion counted on one mbarrier per slot); the
+// row threads read the slots, hand them back through a second mbarrier per
+// slot, and never wait for DRAM directly.  Per row:
+//   1. Window.  The row's first kSampleChunks copies are spread over it
+//      (chunk order (i * nch) / ns first); their maximum m^ fixes the weight
+//      reference and a window of kWinKeys = 2048 consecutive keys, the 16
+//      binades [2^(e-11), 2^(e+5)) around m^ in [2^e, 2^(e+1)).
+//   2. One pass over every slot: the sum of 2^((x - m^) c) (NaN or +inf
+//      anywhere shows in it), the row maximum, and an exact count of every
+//      key in the window (one predicated shared-memory reduction per
+//      element, kCopies interleaved copies of the histogram).  Every key
+//      weighs the same for all of its elements, so the counts give the mass
+//      above any key in the window exactly.  The argmax is not taken: only
+//      greedy rows read it.
+//   3. The nucleus: the key counts walked down from the row maximum in
+//      float-float (as the two-pass route does).
+// A row this route cannot finish exactly (m^ not above zero, a maximum
+// above the window, a boundary below it, a sum that is not finite, a wait
+// that ran out) is marked kRowRedo and the two-pass kernel recomputes it.
+#include "../../include/specverify.h"
+#include "bulk.cuh"
+#include "launch.cuh"
+#include "linear_args.cuh"
+#include "rowstats.cuh"
+
+namespace sv {
+
+constexpr int kChunkBytes = 8192;                    // bytes per bulk copy
+constexpr int kChunkVecs = kChunkBytes / 16;         // 16-byte vectors per copy
+constexpr int kVecsPerThread = kChunkVecs / kNT;
+constexpr int kSlots = 4;                            // ring slots (32 KiB)
+constexpr int kSampleChunks = 2;                     // copies that give m^
+constexpr int kWinKeys = 2048;                       // keys counted in the pass: 16 binades
+constexpr int kWinBelow = 11;                        // binades of the window below m^'s
+constexpr int kCopies = 4;                           // interleaved histogram copies
+constexpr int kOnePassThreads = kNT + 32;            // row threads + the copy warp
+constexpr int kOnePassCtasPerSm = 3;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;     // a wait longer than 2 s is an error
+static_assert(kChunkVecs % kNT == 0, "whole vectors per row thread and copy");
+static_assert((kWinKeys * kCopies) % (4 * kNT) == 0, "histogram cleared in whole uint4 per thread");
+static_assert(kCopies == 4, "the count address assumes 4 copies (16 bytes per key)");
+
+struct OnePassSmem {
+    uint4 ring[kSlots][kChunkVecs];
+    uint32_t hist[kWinKeys * kCopies];  // count of key key_a + p in copy c at [p * kCopies + c]
+    uint64_t full[kSlots];              // slot holds its copy (1 arrival + bytes)
+    uint64_t empty[kSlots];             // slot read by every row warp (kNW arrivals)
+    BlockScratch s;
+    float xtok;
+    int aborted;
+};
+
+__device__ __forceinline__ const __nv_bfloat16* onepass_row(const LinearArgs& a, int r, int& tok) {
+    const int nt = a.B * (a.k + 1);
+    if (r < nt) {
+        const int b = r / (a.k + 1), i = r - b * (a.k + 1);
+        tok = (i < a.k) ? a.drafts[(size_t)b * a.k + i] : -1;
+        return static_cast<const __nv_bfloat16*>(a.tgt) + (size_t)r * a.V;
+    }
+    const int rr = r - nt;
+    tok = a.drafts[rr];
+    return static_cast<const __nv_bfloat16*>(a.drf) + (size_t)rr * a.V;
+}
+
+// A row's copy order: the ns sample chunks (i * nch) / ns first, then the
+// others in increasing order.  f(s, ch) is called for positions s = 0, 1, ...
+// (one division per sample chunk, none per chunk).
+template <typename F>
+__device__ __forceinline__ void for_each_chunk(int nch, int ns, F&& f) {
+    for (int i = 0; i < ns; ++i) f(i, (i * nch) / ns);
+    int s = ns;
+    for (int i = 0; i < ns; ++i) {
+        const int a = (i * nch) / ns + 1, b = (i + 1 < ns) ? ((i + 1) * nch) / ns : nch;
+        for (int ch = a; ch < b; ++ch) f(s++, ch);
+    }
+}
+
+__device__ __forceinline__ __nv_bfloat162 as_bf162(uint32_t w) { return *reinterpret_cast<__nv_bfloat162*>(&w); }
+__device__ __forceinline__ __nv_bfloat162 vec_max(const uint4& q) {
+    return __hmax2(__hmax2(as_bf162(q.x), as_bf162(q.y)), __hmax2(as_bf162(q.z), as_bf162(q.w)));
+}
+
+// Counts element xb (float bit pattern, bf16 bits << 16) at its key's
+// position in the window, clamped: position 0 takes every element at or
+// below the bottom key (negative ones too: as signed integers they sort
+// below every positive pattern), position kWinKeys - 1 every element at or
+// above the top key.  Positions 1 .. kWinKeys - 2 are exact key counts.  No
+// predicate and no branch; hbk is the lane's copy base minus xb_a >> 12, so
+// that the position's 16-byte slot is hbk + (clamped bits >> 12).
+__device__ __forceinline__ void count_key(uint32_t xb, int lo, int hi, uint32_t hbk) {
+    const uint32_t cb = (uint32_t)min(max((int)xb, lo), hi);
+    asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(hbk + (cb >> 12)) : "memory");
+}
+
+__global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_topp_onepass(LinearArgs a) {
+    extern __shared__ __align__(128) uint8_t onepass_raw[];
+    OnePassSmem& sm = *reinterpret_cast<OnePassSmem*>(onepass_raw);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int R = a.B * (2 * a.k + 1);
+    const int V = a.V;
+    volatile int* aborted = &sm.aborted;
+    if (tid == 0) {
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(&sm.full[i], 1);
+            mbar_init(&sm.empty[i], kNW);
+        }
+        sm.aborted = 0;
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == kNW) {  // ---------------------------------------- copy warp
+        if (lane != 0) return;
+        uint32_t g = 0;  // copies issued by this CTA so far
+        bool ok = true;
+        for (int r = blockIdx.x; r < R && ok; r += gridDim.x) {
+            int tok;
+            const RowView<__nv_bfloat16> rv(onepass_row(a, r, tok), V);
+            const int bytes = rv.nvec * 16;
+            const int nch = (bytes + kChunkBytes - 1) / kChunkBytes;
+            const char* base = reinterpret_cast<const char*>(rv.vec());
+            for_each_chunk(nch, min(kSampleChunks, nch), [&](int, int ch) {
+                if (!ok) return;
+                const int slot = (int)(g % kSlots);
+                if (g >= kSlots && !mbar_test(&sm.empty[slot], ((g / kSlots) - 1u) & 1u) &&
+                    !mbar_wait(&sm.empty[slot], ((g / kSlots) - 1u) & 1u, kWaitLimitNs)) {
+                    ok = false;
+                    return;
+                }
+                if (*aborted) {
+                    ok = false;
+                    return;
+                }
+                const int nb = min(kChunkBytes, bytes - ch * kChunkBytes);
+                mbar_arrive_expect_tx(&sm.full[slot], (uint32_t)nb);
+                bulk_load(sm.ring[slot], base + (size_t)ch * kChunkBytes, (uint32_t)nb, &sm.full[slot]);
+                ++g;
+            });
+        }
+        if (!ok) *aborted = 1;
+        // every copy issued has landed before the CTA may end
+        for (uint32_t i = g > (uint32_t)kSlots ? g - kSlots : 0u; i < g; ++i)
+            mbar_wait(&sm.full[i % kSlots], (i / kSlots) & 1u, kWaitLimitNs);
+        return;
+    }
+
+    // ------------------------------------------------------------ row threads
+    const float c = a.c;
+    const float top_p = a.top_p;
+    const uint32_t hb = smem_addr(sm.hist) + 4u * (uint32_t)(lane & (kCopies - 1));
+    uint32_t g0 = 0;  // copies of this CTA's earlier rows
+    bool ab = false;  // this thread saw a wait run out
+    auto wait_full = [&](uint32_t g) {
+        uint64_t* bar = &sm.full[g % kSlots];
+        const uint32_t par = (g / kSlots) & 1u;
+        if (mbar_test(bar, par)) return;
+        if (ab || *aborted) {
+            ab = true;
+            return;
+        }
+        if (!mbar_wait(bar, par, kWaitLimitNs)) {
+            ab = true;
+            *aborted = 1;
+        }
+    };
+
+    for (int r = blockIdx.x; r < R; r += gridDim.x) {
+        int tok;
+        const __nv_bfloat16* row = onepass_row(a, r, tok);
+        const RowView<__nv_bfloat16> rv(row, V);
+        const int nch = (rv.nvec * 16 + kChunkBytes - 1) / kChunkBytes;
+        const int ns = min(kSampleChunks, nch);
+        if (tid == 0) sm.xtok = (tok >= 0 && tok < V) ? ElemT<__nv_bfloat16>::load(row + tok) : __int_as_float(0x7fffffff);
+        const float xh = (tid < rv.head) ? ElemT<__nv_bfloat16>::load(row + tid) : -INFINITY;
+        const float xt = (tid < rv.tail) ? ElemT<__nv_bfloat16>::load(row + rv.head + rv.nvec * 8 + tid) : -INFINITY;
+
+        // 1. m^ over the sample chunks (copy positions 0 .. ns-1), the window
+        __nv_bfloat162 smax = as_bf162(0xff80ff80u);
+        for (int i = 0; i < ns; ++i) {
+            const uint32_t g = g0 + i;
+            wait_full(g);
+            const int ch = (i * nch) / ns;
+            const int nvc = min(kChunkVecs, rv.nvec - ch * kChunkVecs);
+#pragma unroll
+            for (int h = 0; h < kVecsPerThread; ++h) {
+                const int v = tid + h * kNT;
+                if (v < nvc) smax = __hmax2(smax, vec_max(sm.ring[g % kSlots][v]));
+            }
+        }
+        for (int i = tid; i < kWinKeys * kCopies / 4; i += kNT)
+            reinterpret_cast<uint4*>(sm.hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+        const float mh = block_max(fmaxf(__low2float(smax), __high2float(smax)), sm.s);  // also publishes the clear
+        // window [2^(e-11), 2^(e+5)) for m^ in [2^e, 2^(e+1)): bf16 bits of 2^(e-11) are (e - 11 + 127) << 7
+        const int be = (int)((__float_as_uint(mh) >> 23) & 0xffu) - kWinBelow;  // biased exponent of the bottom
+        const bool est = mh > 0.0f && mh < INFINITY && be >= 1;
+        const int key_a = 0x8000 + (be << 7);
+        const uint32_t xba = (uint32_t)max(be, 1) << 23;                    // bits of the bottom key's value
+        const int clo = (int)xba, chi = (int)(xba + ((uint32_t)(kWinKeys - 1) << 16));  // bottom and top keys' bits
+        const uint32_t hbk = hb - (xba >> 12);
+
+        // 2. the pass: copy positions 0 .. nch-1 (the sample chunks again first)
+        const float rc = est ? mh * c : 0.0f;
+        const float2 cc = make_float2(c, c), nrc = make_float2(-rc, -rc);
+        float zs = 0.0f, zc = 0.0f;  // Kahan pair over chunks
+        auto take_vec = [&](const uint4& q, float2& za) {
+            const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t xl = w4[j] << 16, xu = w4[j] & 0xffff0000u;
+                const float2 t = __ffma2_rn(make_float2(__uint_as_float(xl), __uint_as_float(xu)), cc, nrc);
+                za = __fadd2_rn(za, make_float2(ex2(t.x), ex2(t.y)));
+                count_key(xl, clo, chi, hbk);
+                count_key(xu, clo, chi, hbk);
+            }
+        };
+        for_each_chunk(nch, ns, [&](int s, int ch) {
+            const uint32_t g = g0 + (uint32_t)s;
+            wait_full(g);
+            const uint4* slot = sm.ring[g % kSlots];
+            float2 za0 = make_float2(0.0f, 0.0f), za1 = za0;
+            const int nvc = min(kChunkVecs, rv.nvec - ch * kChunkVecs);
+            if (nvc == kChunkVecs) {
+                const uint4 q0 = slot[tid], q1 = slot[tid + kNT];
+                take_vec(q0, za0);
+                take_vec(q1, za1);
+            } else {
+                if (tid < nvc) take_vec(slot[tid], za0);
+                if (tid + kNT < nvc) take_vec(slot[tid + kNT], za1);
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.empty[g % kSlots]);
+            const float y = ((za0.x + za1.x) + (za0.y + za1.y)) - zc;
+            const float tt = zs + y;
+            zc = (tt - zs) - y;
+            zs = tt;
+        });
+        static_assert(kVecsPerThread == 2, "the pass takes two vectors per thread and copy");
+        g0 += (uint32_t)nch;
+        auto take_scalar = [&](float x) {
+            zs += ex2(fmaf(x, c, -rc));
+            count_key(__float_as_uint(x), clo, chi, hbk);
+        };
+        if (tid < rv.head) take_scalar(xh);
+        if (tid < rv.tail) take_scalar(xt);
+
+        // 3. block results; NaN or +inf anywhere makes the sum NaN or +inf
+        const bool abort_row = row_sync_or(ab || *aborted);
+        const ff zr = block_sum_ff(ff_add(ff{zs, 0.0f}, ff{-zc, 0.0f}), sm.s);  // its barriers publish the counts
+        // merge the copies; the highest nonempty position gives the maximum
+        uint32_t sum[kWinKeys / kNT];
+        int ptop = -1;
+#pragma unroll
+        for (int i = 0; i < kWinKeys / kNT; ++i) {
+            const int p = tid + i * kNT;
+            const uint4 q = reinterpret_cast<const uint4*>(sm.hist)[p];
+            sum[i] = (q.x + q.y) + (q.z + q.w);
+            if (sum[i] != 0u) ptop = p;
+        }
+        ptop = -block_min_i(-ptop, sm.s);  // also: every copy has been read
+#pragma unroll
+        for (int i = 0; i < kWinKeys / kNT; ++i) sm.hist[tid + i * kNT] = sum[i];
+        const float xtk = sm.xtok;
+        row_sync();
+
+        RowStat st;
+        st.argmax = 0;  // read for greedy rows only
+        st.tau = -INFINITY;
+        st.n_keep = 0;
+        st.c_tau = 0;
+        st.inv_zn = 0.0f;
+        st.x_tok = xtk;
+        st.flags = 0;
+        // leave to the two-pass route: no window, a maximum at or above the
+        // window's top key, nothing above its bottom key, a sum that is not
+        // finite and positive (NaN, +inf, or weights too large for fp32
+        // relative to m^)
+        const int kmax = key_a + ptop;
+        const float M = key_value(kmax);
+        st.m = M;
+        bool redo = abort_row || !est || ptop <= 0 || ptop >= kWinKeys - 1 ||
+                    !(zr.hi > 0.0f && zr.hi < INFINITY) || (M - mh) * c > 96.0f;
+        if (!redo) {
+            const ff Z = ff_scale(zr, ex2((mh - M) * c));
+            const float mc = scaled_max(M, c);
+            const ff pZ = ff_mul_f(Z, top_p);
+            // positions 1 .. ptop, walked down from the maximum (warp 0 alone
+            // for short windows, the block for longer ones)
+            ff F_end;
+            const WalkOut o =
+                (ptop <= 256)
+                    ? walk_keys<true, true>(sm.hist + 1, ptop, plain_map(kmax), c, mc, ff{0.0f, 0.0f}, pZ, &F_end, sm.s)
+                    : walk_keys<false, true>(sm.hist + 1, ptop, plain_map(kmax), c, mc, ff{0.0f, 0.0f}, pZ, &F_end, sm.s);
+            if (o.found != 1) {
+                redo = true;  // the boundary lies at or below the bottom key
+            } else {
+                st.tau = o.r.tau;
+                st.n_keep = o.r.n_keep;
+                st.c_tau = o.r.c_tau;
+                bool member;
+                if (xtk == st.tau && o.r.n_keep < o.r.c_tau) {
+                    int before = 0;
+                    row_find_nth_equal<__nv_bfloat16>(row, V, st.tau, -1, tok, &before, sm.s,
+                                                      *reinterpret_cast<SampleScratch*>(sm.hist));
+                    member = before < o.r.n_keep;
+                } else {
+                    member = xtk >= st.tau;
+                }
+                st.inv_zn = 1.0f / ff_to_float(o.r.mass);
+                st.flags = member ? kRowTokMember : 0;
+            }
+        }
+        if (redo) st.flags = kRowRedo;
+        if (tid == 0) a.stats[r] = st;
+        if (abort_row) {  // leave every remaining row to the two-pass kernel
+            if (tid == 0) {
+                if (a.dev_error) atomicOr(a.dev_error, kDevErrTimeout);
+                for (int r2 = r + gridDim.x; r2 < R; r2 += gridDim.x) a.stats[r2].flags = kRowRedo;
+            }
+            break;
+        }
+        row_sync();  // the histogram and the scratch are cleared for the next row
+    }
+}
+
+spec_status launch_rows_topp_onepass(LinearArgs& a, cudaStream_t st) {
+    const long long R = (long long)a.B * (2 * a.k + 1);
+    const size_t smem = sizeof(OnePassSmem);
+    int grid = 0;
+    if (!launch_grid(k_rows_topp_onepass, smem, R, &grid, kOnePassThreads)) return SPEC_ERR_CUDA;
+    k_rows_topp_onepass<<<grid, kOnePassThreads, smem, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+}  // namespace sv

@@ -135,7 +135,7 @@ __device__ __forceinline__ Pass1 reduce_pass1(float m, ff z, int idx, bool bad, 
         s.pi[w] = idx;
         s.pi2[w] = bw;
     }
-    __syncthreads();
+    row_sync();
     if (w == 0) {
         const float mi = (lane < kNW) ? s.pf[lane] : -INFINITY;
         const float M = warp_max(mi);
@@ -155,7 +155,7 @@ __device__ __forceinline__ Pass1 reduce_pass1(float m, ff z, int idx, bool bad, 
             s.ri[kNW + 1] = Bd;
         }
     }
-    __syncthreads();
+    row_sync();
     Pass1 r;
     r.m = s.rf[kNW];
     r.z = ff{s.rf[kNW + 1], s.rf2[kNW]};
@@ -184,7 +184,7 @@ __device__ Pass1 row_pass1(const T* __restrict__ row, int V, float c, BlockScrat
         const int nslots = min(kSampleCap, 2 * kNT * ((rv.nvec + kUnroll * kNT - 1) / (kUnroll * kNT)));
         for (int i = tid; i < (nslots + 7) / 8; i += kNT)
             reinterpret_cast<uint4*>(sample)[i] = make_uint4(0x7fff7fffu, 0x7fff7fffu, 0x7fff7fffu, 0x7fff7fffu);
-        __syncthreads();
+        row_sync();
     }
     auto take_scalar = [&](float x) {
         bad |= (x != x);
@@ -348,7 +348,7 @@ __device__ int row_find_nth_equal(const T* __restrict__ row, int V, float val, i
         c = warp_sum_i(c);
         if (lane == 0) sc[st] = c;
     }
-    __syncthreads();
+    row_sync();
     if (warp == 0) {
         const int per = (nsteps + 31) / 32;
         int ls = 0;
@@ -397,10 +397,10 @@ __device__ int row_find_nth_equal(const T* __restrict__ row, int V, float val, i
             s.bcast_i[6] = found;
         }
     }
-    __syncthreads();
+    row_sync();
     const int r = s.bcast_i[6];
     if (count) *count = s.bcast_i[5];
-    __syncthreads();
+    row_sync();
     return r;
 }
 
@@ -586,7 +586,7 @@ __device__ WalkOut walk_keys(const uint32_t* hist, int nbins, const WalkMap& map
         s.bcast_f[3] = tot.hi;
         s.bcast_f[4] = tot.lo;
     }
-    __syncthreads();
+    row_sync();
     WalkOut o;
     o.found = s.bcast_i[0];
     o.r.tau = s.bcast_f[0];
@@ -595,7 +595,7 @@ __device__ WalkOut walk_keys(const uint32_t* hist, int nbins, const WalkMap& map
     o.r.c_tau = s.bcast_i[2];
     o.F_lump = o.r.mass;
     if (F_end) *F_end = ff_add(F0, ff{s.bcast_f[3], s.bcast_f[4]});
-    __syncthreads();
+    row_sync();
     return o;
 }
 
@@ -631,7 +631,7 @@ __device__ inline void count_key_window(const __nv_bfloat16* __restrict__ row, i
         }
     }
     if (tid < rv.tail) take(*reinterpret_cast<const unsigned short*>(row + rv.head + rv.nvec * 8 + tid));
-    __syncthreads();
+    row_sync();
     if (tid == 0 && khi >= 0x8000 && klo <= 0x7fff) {
         hist[khi - 0x8000] += hist[khi - 0x7fff];
         hist[khi - 0x7fff] = 0u;
@@ -711,7 +711,7 @@ __device__ inline void merge_copies8(uint32_t* hist, int nb) {
             sum[j] = (a.x + a.y) + (a.z + a.w) + (b.x + b.y) + (b.z + b.w);
         }
     }
-    __syncthreads();
+    row_sync();
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const int i = threadIdx.x + j * kNT;
@@ -726,14 +726,14 @@ __device__ inline void count_window_one_sign(const __nv_bfloat16* __restrict__ r
     const int nb = khi - klo + 1;
     if (nb <= 4 * kNT && 8 * nb <= kFullBins) {
         for (int i = threadIdx.x; i < 8 * nb; i += kNT) hist[i] = 0u;
-        __syncthreads();
+        row_sync();
         if (top) count_window_signed<NEG, true, 8>(row, V, klo, khi, hist);
         else count_window_signed<NEG, false, 8>(row, V, klo, khi, hist);
-        __syncthreads();
+        row_sync();
         merge_copies8(hist, nb);
     } else {
         for (int i = threadIdx.x; i < nb; i += kNT) hist[i] = 0u;
-        __syncthreads();
+        row_sync();
         if (top) count_window_signed<NEG, true, 1>(row, V, klo, khi, hist);
         else count_window_signed<NEG, false, 1>(row, V, klo, khi, hist);
     }
@@ -760,10 +760,10 @@ __device__ inline Topp topp_windows(const __nv_bfloat16* __restrict__ row, int V
             count_window_one_sign<true>(row, V, lo, hi, at_top, hist);
         } else {
             for (int i = threadIdx.x; i < nb; i += kNT) hist[i] = 0u;
-            __syncthreads();
+            row_sync();
             count_key_window(row, V, lo, hi, hist);
         }
-        __syncthreads();
+        row_sync();
         ff F_end;
         WalkOut o;
         if (pos) {  // warp 0 alone walks short windows; the block walks longer ones
@@ -983,7 +983,7 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
             reinterpret_cast<uint4*>(scount)[i] = make_uint4(0u, 0u, 0u, 0u);
             reinterpret_cast<uint4*>(tcount)[i] = make_uint4(0u, 0u, 0u, 0u);
         }
-        __syncthreads();
+        row_sync();
         auto bin_of = [&](float x) {
             const int j = (int)((m - x) * inv_w);
             return j < 0 ? 0 : (j > kEstBins - 1 ? kEstBins - 1 : j);
@@ -1016,7 +1016,7 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
             s.pf[warp] = gb;
             s.pf2[warp] = vb;
         }
-        __syncthreads();  // also publishes the bins
+        row_sync();  // also publishes the bins
         int S = 0;
         float Gb = 0.0f, Vb = 0.0f;
         for (int w = 0; w < kNW; ++w) {  // same order in every thread: identical values
@@ -1056,7 +1056,7 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
         }
         float4* wtot = reinterpret_cast<float4*>(smem + kWTotOffset);
         if (lane == 31) wtot[warp] = inc;
-        __syncthreads();
+        row_sync();
         float4 base = make_float4(0.0f, 0.0f, 0.0f, 0.0f), all = base;
         for (int w = 0; w < kNW; ++w) {
             const float4 t = wtot[w];
@@ -1085,7 +1085,7 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
         }
         int r1 = warp_min_i(jp), r2 = -warp_min_i(-j0);
         if (lane == 0) { s.pi[warp] = r1; s.pi2[warp] = r2; }
-        __syncthreads();
+        row_sync();
         int Jp = 0x7fffffff, J0 = -1;
         for (int w = 0; w < kNW; ++w) { Jp = min(Jp, s.pi[w]); J0 = max(J0, s.pi2[w]); }
         // the owners of bins Jp + 2 and J0 publish the sample count and the squares there
@@ -1101,7 +1101,7 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
             }
             if (tid == 0 && J0 == kEstBins) s.bcast_f[6] = Vb;
         }
-        __syncthreads();
+        row_sync();
         const float ns = s.bcast_f[5], v0 = s.bcast_f[6];
         if (Jp != 0x7fffffff && (S < 256 || 16.0f * ns <= (float)S)) {
             route = 1;
@@ -1126,9 +1126,9 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
             if (tid == 0 && Gb >= Tb) jb = max(jb, kEstBins);
             r1 = -warp_min_i(-ja);
             r2 = -warp_min_i(-jb);
-            __syncthreads();  // everyone has read the previous partials
+            row_sync();  // everyone has read the previous partials
             if (lane == 0) { s.pi[warp] = r1; s.pi2[warp] = r2; }
-            __syncthreads();
+            row_sync();
             int JA = -1, JB = -1;
             for (int w = 0; w < kNW; ++w) { JA = max(JA, s.pi[w]); JB = max(JB, s.pi2[w]); }
             // one bin of slack on each side
@@ -1148,7 +1148,7 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
                 key_b = kb;
             }
         }
-        __syncthreads();  // the estimate's shared memory becomes the histogram
+        row_sync();  // the estimate's shared memory becomes the histogram
     }
     if (route == 1) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_a, ff{0.0f, 0.0f}, hist, s, 0, true);
     if (route == 0) return topp_windows(row, V, c, mc, Z, pZ, kmax, key_lo, ff{0.0f, 0.0f}, hist, s, 0, true);
@@ -1160,7 +1160,7 @@ __device__ inline Topp row_topp_bf16(const __nv_bfloat16* __restrict__ row, int 
     const MixedLayout L(key_a, key_b);
     const int W = spans ? L.bins() : key_b - key_a + 1;
     for (int i = tid; i < W; i += kNT) hist[i] = 0u;
-    __syncthreads();
+    row_sync();
     ff part, lpart = ff{0.0f, 0.0f};
     if (!spans) part = band_pass_neg(row, V, c, mc, key_a, key_b, hist);
     else band_pass_mixed(row, V, c, mc, L, hist, part, lpart);

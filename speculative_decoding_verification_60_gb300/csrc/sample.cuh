@@ -49,7 +49,7 @@ __device__ int block_inverse_cdf(int units, float u, const WeightFn& wf, BlockSc
             ss.sl[st] = t.lo;
         }
     }
-    __syncthreads();
+    row_sync();
     // B + C: warp 0 finds the crossing step and walks it
     if (warp == 0) {
         const int per = (nsteps + 31) / 32;
@@ -137,9 +137,9 @@ __device__ int block_inverse_cdf(int units, float u, const WeightFn& wf, BlockSc
         }
         if (lane == 0) s.bcast_i[7] = pick;
     }
-    __syncthreads();
+    row_sync();
     const int r = s.bcast_i[7];
-    __syncthreads();
+    row_sync();
     return r;
 }
 
@@ -401,7 +401,7 @@ __device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<
             ds.cq[st] = nq;
         }
     }
-    __syncthreads();
+    row_sync();
     // B1: the steps holding the cuts (warp 0): the n_keep-th tau-valued token of each row
     if (warp == 0) {
         auto cut_step = [&](const int* cnts, int n, int& js, int& pre) {
@@ -439,9 +439,9 @@ __device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<
             s.bcast_i[3] = preq;
         }
     }
-    __syncthreads();
+    row_sync();
     const int jsp = s.bcast_i[0], prep = s.bcast_i[1], jsq = s.bcast_i[2], preq = s.bcast_i[3];
-    __syncthreads();
+    row_sync();
     // B2: the cut index inside its step, one 32-unit sub-step per warp
     auto locate = [&](int js, int pre, int n, const FilteredRow<T>& R, float tau) -> int {
         unsigned msk = 0u;
@@ -459,7 +459,7 @@ __device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<
             if (lane == 0) ds.sub_i[warp] = c;
         }
         if (threadIdx.x == 0) s.bcast_i[4] = 0x7fffffff;
-        __syncthreads();
+        row_sync();
         int base = pre, gsel = -1, gpre = 0;
         for (int g = 0; g < kSub; ++g) {
             if (gsel < 0 && base + ds.sub_i[g] > n) { gsel = g; gpre = base; }
@@ -477,9 +477,9 @@ __device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<
                     }
             }
         }
-        __syncthreads();
+        row_sync();
         const int r = s.bcast_i[4];
-        __syncthreads();
+        row_sync();
         return r;
     };
     if (jsp >= 0) P.cut = locate(jsp, prep, P.st.n_keep - 1, P, tp);
@@ -502,10 +502,10 @@ __device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<
                 ds.sub_l[warp] = t.lo;
             }
         }
-        __syncthreads();
+        row_sync();
         ff r = ff{0.0f, 0.0f};
         for (int g = 0; g < kSub; ++g) r = ff_add(r, ff{ds.sub_h[g], ds.sub_l[g]});
-        __syncthreads();
+        row_sync();
         return r;
     };
     const ff exact_p = (jsp >= 0) ? exact_step(jsp) : ff{0.0f, 0.0f};
@@ -576,11 +576,11 @@ __device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<
             s.bcast_f[3] = tgt.lo;
         }
     }
-    __syncthreads();
+    row_sync();
     const int js = s.bcast_i[5];
     const ff tgt = ff{s.bcast_f[2], s.bcast_f[3]};
     ff run = ff{s.bcast_f[0], s.bcast_f[1]};
-    __syncthreads();
+    row_sync();
     if (js < 0) return -1;  // every weight is zero
     // C: the crossing step, one sub-step per warp
     float w[VEC];
@@ -608,7 +608,7 @@ __device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<
             ds.sub_j[warp] = mylast;
         }
     }
-    __syncthreads();
+    row_sync();
     int g_cross = -1, lastw = -1;
     ff pre_cross = run;
     for (int g = 0; g < kSub; ++g) {  // the same order in every warp
@@ -643,9 +643,9 @@ __device__ int draw_linear(const RowView<T>& rv, FilteredRow<T>& P, FilteredRow<
         }
         if (lane == 0) s.bcast_i[6] = p;
     }
-    __syncthreads();
+    row_sync();
     const int r = s.bcast_i[6];
-    __syncthreads();
+    row_sync();
     return r;
 }
 
