@@ -34,20 +34,33 @@
 
 namespace sv {
 
-constexpr int kChunkBytes = 8192;                    // bytes per bulk copy
+#ifndef SV_ONEPASS_CHUNK
+#define SV_ONEPASS_CHUNK 12288
+#endif
+#ifndef SV_ONEPASS_SLOTS
+#define SV_ONEPASS_SLOTS 3
+#endif
+#ifndef SV_ONEPASS_CTAS
+#define SV_ONEPASS_CTAS 4
+#endif
+constexpr int kChunkBytes = SV_ONEPASS_CHUNK;        // bytes per bulk copy
 constexpr int kChunkVecs = kChunkBytes / 16;         // 16-byte vectors per copy
 constexpr int kVecsPerThread = kChunkVecs / kNT;
-constexpr int kSlots = 4;                            // ring slots (32 KiB)
+constexpr int kSlots = SV_ONEPASS_SLOTS;             // ring slots
 constexpr int kSampleChunks = 2;                     // copies that give m^
 constexpr int kWinKeys = 2048;                       // keys counted in the pass: 16 binades
 constexpr int kWinBelow = 11;                        // binades of the window below m^'s
-constexpr int kCopies = 4;                           // interleaved histogram copies
+#ifndef SV_ONEPASS_COPIES
+#define SV_ONEPASS_COPIES 1
+#endif
+constexpr int kCopies = SV_ONEPASS_COPIES;           // interleaved histogram copies
+constexpr int kCopyShift = (kCopies == 4) ? 12 : (kCopies == 2 ? 13 : 14);  // bits >> kCopyShift = key bytes
 constexpr int kOnePassThreads = kNT + 32;            // row threads + the copy warp
-constexpr int kOnePassCtasPerSm = 3;
+constexpr int kOnePassCtasPerSm = SV_ONEPASS_CTAS;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;     // a wait longer than 2 s is an error
 static_assert(kChunkVecs % kNT == 0, "whole vectors per row thread and copy");
 static_assert((kWinKeys * kCopies) % (4 * kNT) == 0, "histogram cleared in whole uint4 per thread");
-static_assert(kCopies == 4, "the count address assumes 4 copies (16 bytes per key)");
+static_assert(kCopies == 1 || kCopies == 2 || kCopies == 4, "1, 2 or 4 copies (4 * kCopies bytes per key)");
 
 struct OnePassSmem {
     uint4 ring[kSlots][kChunkVecs];
@@ -98,7 +111,7 @@ __device__ __forceinline__ __nv_bfloat162 vec_max(const uint4& q) {
 // that the position's 16-byte slot is hbk + (clamped bits >> 12).
 __device__ __forceinline__ void count_key(uint32_t xb, int lo, int hi, uint32_t hbk) {
     const uint32_t cb = (uint32_t)min(max((int)xb, lo), hi);
-    asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(hbk + (cb >> 12)) : "memory");
+    asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(hbk + (cb >> kCopyShift)) : "memory");
 }
 
 __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_topp_onepass(LinearArgs a) {
@@ -159,9 +172,7 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
     const uint32_t hb = smem_addr(sm.hist) + 4u * (uint32_t)(lane & (kCopies - 1));
     uint32_t g0 = 0;  // copies of this CTA's earlier rows
     bool ab = false;  // this thread saw a wait run out
-    auto wait_full = [&](uint32_t g) {
-        uint64_t* bar = &sm.full[g % kSlots];
-        const uint32_t par = (g / kSlots) & 1u;
+    auto wait_full = [&](uint64_t* bar, uint32_t par) {
         if (mbar_test(bar, par)) return;
         if (ab || *aborted) {
             ab = true;
@@ -187,7 +198,7 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
         __nv_bfloat162 smax = as_bf162(0xff80ff80u);
         for (int i = 0; i < ns; ++i) {
             const uint32_t g = g0 + i;
-            wait_full(g);
+            wait_full(&sm.full[g % kSlots], (g / kSlots) & 1u);
             const int ch = (i * nch) / ns;
             const int nvc = min(kChunkVecs, rv.nvec - ch * kChunkVecs);
 #pragma unroll
@@ -205,48 +216,57 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
         const int key_a = 0x8000 + (be << 7);
         const uint32_t xba = (uint32_t)max(be, 1) << 23;                    // bits of the bottom key's value
         const int clo = (int)xba, chi = (int)(xba + ((uint32_t)(kWinKeys - 1) << 16));  // bottom and top keys' bits
-        const uint32_t hbk = hb - (xba >> 12);
+        const uint32_t hbk = hb - (xba >> kCopyShift);
 
-        // 2. the pass: copy positions 0 .. nch-1 (the sample chunks again first)
+        // 2. the pass: copy positions 0 .. nch-1 (the sample chunks again first).
+        // Each thread keeps one pair of partial sums per vector slot of a
+        // chunk over the whole row (about V / (2 kNT kVecsPerThread) terms
+        // each), merged in float-float at the end.
         const float rc = est ? mh * c : 0.0f;
         const float2 cc = make_float2(c, c), nrc = make_float2(-rc, -rc);
-        float zs = 0.0f, zc = 0.0f;  // Kahan pair over chunks
-        auto take_vec = [&](const uint4& q, float2& za) {
+        float2 za[kVecsPerThread];
+#pragma unroll
+        for (int h = 0; h < kVecsPerThread; ++h) za[h] = make_float2(0.0f, 0.0f);
+        auto take_vec = [&](const uint4& q, float2& acc) {
             const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const uint32_t xl = w4[j] << 16, xu = w4[j] & 0xffff0000u;
                 const float2 t = __ffma2_rn(make_float2(__uint_as_float(xl), __uint_as_float(xu)), cc, nrc);
-                za = __fadd2_rn(za, make_float2(ex2(t.x), ex2(t.y)));
+                acc = __fadd2_rn(acc, make_float2(ex2(t.x), ex2(t.y)));
                 count_key(xl, clo, chi, hbk);
                 count_key(xu, clo, chi, hbk);
             }
         };
-        for_each_chunk(nch, ns, [&](int s, int ch) {
-            const uint32_t g = g0 + (uint32_t)s;
-            wait_full(g);
-            const uint4* slot = sm.ring[g % kSlots];
-            float2 za0 = make_float2(0.0f, 0.0f), za1 = za0;
-            const int nvc = min(kChunkVecs, rv.nvec - ch * kChunkVecs);
-            if (nvc == kChunkVecs) {
-                const uint4 q0 = slot[tid], q1 = slot[tid + kNT];
-                take_vec(q0, za0);
-                take_vec(q1, za1);
+        const int nvc_last = rv.nvec - (nch - 1) * kChunkVecs;  // vectors of the last chunk (only it can be short)
+        uint32_t slot = g0 % kSlots, par = (g0 / kSlots) & 1u;
+        for_each_chunk(nch, ns, [&](int, int ch) {
+            wait_full(&sm.full[slot], par);
+            const uint4* sp = sm.ring[slot];
+            if (ch != nch - 1 || nvc_last == kChunkVecs) {
+                uint4 q[kVecsPerThread];
+#pragma unroll
+                for (int h = 0; h < kVecsPerThread; ++h) q[h] = sp[tid + h * kNT];
+#pragma unroll
+                for (int h = 0; h < kVecsPerThread; ++h) take_vec(q[h], za[h]);
             } else {
-                if (tid < nvc) take_vec(slot[tid], za0);
-                if (tid + kNT < nvc) take_vec(slot[tid + kNT], za1);
+#pragma unroll
+                for (int h = 0; h < kVecsPerThread; ++h)
+                    if (tid + h * kNT < nvc_last) take_vec(sp[tid + h * kNT], za[h]);
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.empty[g % kSlots]);
-            const float y = ((za0.x + za1.x) + (za0.y + za1.y)) - zc;
-            const float tt = zs + y;
-            zc = (tt - zs) - y;
-            zs = tt;
+            if (lane == 0) mbar_arrive(&sm.empty[slot]);
+            if (++slot == kSlots) {
+                slot = 0;
+                par ^= 1u;
+            }
         });
-        static_assert(kVecsPerThread == 2, "the pass takes two vectors per thread and copy");
         g0 += (uint32_t)nch;
+        ff zsum = ff{0.0f, 0.0f};
+#pragma unroll
+        for (int h = 0; h < kVecsPerThread; ++h) zsum = ff_add(zsum, ff_add(ff{za[h].x, 0.0f}, ff{za[h].y, 0.0f}));
         auto take_scalar = [&](float x) {
-            zs += ex2(fmaf(x, c, -rc));
+            zsum = ff_add_f(zsum, ex2(fmaf(x, c, -rc)));
             count_key(__float_as_uint(x), clo, chi, hbk);
         };
         if (tid < rv.head) take_scalar(xh);
@@ -254,15 +274,17 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
 
         // 3. block results; NaN or +inf anywhere makes the sum NaN or +inf
         const bool abort_row = row_sync_or(ab || *aborted);
-        const ff zr = block_sum_ff(ff_add(ff{zs, 0.0f}, ff{-zc, 0.0f}), sm.s);  // its barriers publish the counts
+        const ff zr = block_sum_ff(zsum, sm.s);  // its barriers publish the counts
         // merge the copies; the highest nonempty position gives the maximum
         uint32_t sum[kWinKeys / kNT];
         int ptop = -1;
 #pragma unroll
         for (int i = 0; i < kWinKeys / kNT; ++i) {
             const int p = tid + i * kNT;
-            const uint4 q = reinterpret_cast<const uint4*>(sm.hist)[p];
-            sum[i] = (q.x + q.y) + (q.z + q.w);
+            uint32_t t = 0u;
+#pragma unroll
+            for (int cpy = 0; cpy < kCopies; ++cpy) t += sm.hist[p * kCopies + cpy];
+            sum[i] = t;
             if (sum[i] != 0u) ptop = p;
         }
         ptop = -block_min_i(-ptop, sm.s);  // also: every copy has been read
