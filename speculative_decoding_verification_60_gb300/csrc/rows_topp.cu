@@ -275,25 +275,25 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
         // 3. block results; NaN or +inf anywhere makes the sum NaN or +inf
         const bool abort_row = row_sync_or(ab || *aborted);
         const ff zr = block_sum_ff(zsum, sm.s);  // its barriers publish the counts
-        // merge the copies; the highest nonempty position gives the maximum
-        uint32_t sum[kWinKeys / kNT];
-        int ptop = -1;
+        if constexpr (kCopies > 1) {  // merge the copies into positions 0 .. kWinKeys-1
+            uint32_t sum[kWinKeys / kNT];
 #pragma unroll
-        for (int i = 0; i < kWinKeys / kNT; ++i) {
-            const int p = tid + i * kNT;
-            uint32_t t = 0u;
+            for (int i = 0; i < kWinKeys / kNT; ++i) {
+                const int p = tid + i * kNT;
+                uint32_t t = 0u;
 #pragma unroll
-            for (int cpy = 0; cpy < kCopies; ++cpy) t += sm.hist[p * kCopies + cpy];
-            sum[i] = t;
-            if (sum[i] != 0u) ptop = p;
+                for (int cpy = 0; cpy < kCopies; ++cpy) t += sm.hist[p * kCopies + cpy];
+                sum[i] = t;
+            }
+            row_sync();
+#pragma unroll
+            for (int i = 0; i < kWinKeys / kNT; ++i) sm.hist[tid + i * kNT] = sum[i];
+            row_sync();
         }
-        ptop = -block_min_i(-ptop, sm.s);  // also: every copy has been read
-#pragma unroll
-        for (int i = 0; i < kWinKeys / kNT; ++i) sm.hist[tid + i * kNT] = sum[i];
         const float xtk = sm.xtok;
-        row_sync();
 
         RowStat st;
+        st.m = mh;      // the weight reference: weights are 2^((x - m^) c)
         st.argmax = 0;  // read for greedy rows only
         st.tau = -INFINITY;
         st.n_keep = 0;
@@ -301,26 +301,20 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
         st.inv_zn = 0.0f;
         st.x_tok = xtk;
         st.flags = 0;
-        // leave to the two-pass route: no window, a maximum at or above the
-        // window's top key, nothing above its bottom key, a sum that is not
-        // finite and positive (NaN, +inf, or weights too large for fp32
-        // relative to m^)
-        const int kmax = key_a + ptop;
-        const float M = key_value(kmax);
-        st.m = M;
-        bool redo = abort_row || !est || ptop <= 0 || ptop >= kWinKeys - 1 ||
-                    !(zr.hi > 0.0f && zr.hi < INFINITY) || (M - mh) * c > 96.0f;
+        // leave to the two-pass route: no window, an element at or above the
+        // window's top key, a sum that is not finite and positive (NaN, +inf,
+        // or weights too large for fp32 relative to m^); a finite sum also
+        // bounds every key's mass below
+        bool redo = abort_row || !est || sm.hist[kWinKeys - 1] != 0u || !(zr.hi > 0.0f && zr.hi < INFINITY);
         if (!redo) {
-            const ff Z = ff_scale(zr, ex2((mh - M) * c));
-            const float mc = scaled_max(M, c);
-            const ff pZ = ff_mul_f(Z, top_p);
-            // positions 1 .. ptop, walked down from the maximum (warp 0 alone
-            // for short windows, the block for longer ones)
+            const float mc = scaled_max(mh, c);
+            const ff pZ = ff_mul_f(zr, top_p);
+            // positions 1 .. kWinKeys-2 walked down from the top by the block
+            // (empty positions cost a load)
+            const int ktop = key_a + kWinKeys - 2;
             ff F_end;
-            const WalkOut o =
-                (ptop <= 256)
-                    ? walk_keys<true, true>(sm.hist + 1, ptop, plain_map(kmax), c, mc, ff{0.0f, 0.0f}, pZ, &F_end, sm.s)
-                    : walk_keys<false, true>(sm.hist + 1, ptop, plain_map(kmax), c, mc, ff{0.0f, 0.0f}, pZ, &F_end, sm.s);
+            const WalkOut o = walk_keys<false, true>(sm.hist + 1, kWinKeys - 2, plain_map(ktop), c, mc, ff{0.0f, 0.0f},
+                                                     pZ, &F_end, sm.s);
             if (o.found != 1) {
                 redo = true;  // the boundary lies at or below the bottom key
             } else {
@@ -349,7 +343,8 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
             }
             break;
         }
-        row_sync();  // the histogram and the scratch are cleared for the next row
+        // the walk and the boundary search end on a barrier, so the next row
+        // may clear the histogram and overwrite xtok right away
     }
 }
 
