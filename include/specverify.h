@@ -38,6 +38,9 @@
  *    that sit within rounding of a threshold can differ.
  *  - Calls that overlap on the GPU must not share output or workspace
  *    buffers.
+ *  - Each call makes the device that holds its logits (or hidden states)
+ *    current for its own launches and puts the caller's current device
+ *    back before it returns.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
@@ -82,7 +85,8 @@ typedef enum { SPEC_OP_LINEAR = 0, SPEC_OP_TREE = 1 } spec_op;
 /* Bits OR-ed into *dev_error. */
 #define SPEC_DEVERR_TOKEN 1      /* a draft/node token outside [0, V) */
 #define SPEC_DEVERR_NONFINITE 2  /* NaN or +inf logit, or no finite logit in a row */
-#define SPEC_DEVERR_PARENT 4     /* parent[] not a tree rooted at 0 with parent[i] < i, or deeper than max_depth */
+#define SPEC_DEVERR_PARENT 4     /* parent[] not a tree rooted at 0 with parent[i] < i, deeper than max_depth,
+                                    or a node with more than 64 children */
 #define SPEC_DEVERR_LENGTH 8     /* compaction: accepted length or source row out of range */
 #define SPEC_DEVERR_TIMEOUT 16   /* a wait for a bulk copy ran out (2 s); the rows it left were
                                     recomputed by the two-pass route, so the results stand */
@@ -122,7 +126,10 @@ size_t spec_workspace_size(spec_op op, int B, int k_or_N, int V, spec_dtype dtyp
  *  = the top-p nucleus in (logit desc, index asc) order (a token is kept
  *  when the mass before it is < top_p), renormalised.
  *  Sampled (T > 0): d_i is accepted iff u_i < p_{i-1}(d_i) / q_{i-1}(d_i)
- *  (q == 0 rejects), u_i from purpose ACCEPT; a = number of leading
+ *  (q == 0, a token outside q's nucleus, rejects; the ratio is taken from
+ *  the logits' exponents when p or q only underflows fp32, so drafts far in
+ *  the tail are decided by their true ratio), u_i from purpose ACCEPT; a =
+ *  number of leading
  *  accepts.  If a < k, t* is the smallest v with C(v) > u * C(V-1), C the
  *  running sum of max(0, p_a - q_a) in index order and u from purpose
  *  RESIDUAL (if that residual is all zero, of p_a instead); if a == k, the

@@ -82,6 +82,7 @@ extern "C" spec_status spec_compact_accepted(const void* hidden, int B, int T, i
                                              const int32_t* path_nodes, const int32_t* out_tokens, int W,
                                              void* out_hidden, int32_t* offsets, int32_t* next_tokens,
                                              int32_t* dev_error, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
     if (!hidden || !accepted_len || !out_tokens || !out_hidden || !offsets || !next_tokens)
         return SPEC_ERR_INVALID_ARG;
     if (B < 1 || T < 1 || H < 1 || W < 1) return SPEC_ERR_INVALID_ARG;

@@ -48,9 +48,20 @@ __global__ void __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
                     qq = 1.0f;
                 } else {
                     const RowStat sq = a.stats[drf_row(a, b, i)];
-                    pp = (sp.flags & kRowTokMember) ? weight_of(sp.x_tok, a.c, scaled_max(sp.m, a.c)) * sp.inv_zn : 0.0f;
-                    qq = (sq.flags & kRowTokMember) ? weight_of(sq.x_tok, a.c, scaled_max(sq.m, a.c)) * sq.inv_zn : 0.0f;
-                    const float ratio = qq > 0.0f ? pp / qq : 0.0f;
+                    const bool pm = (sp.flags & kRowTokMember) != 0, qm = (sq.flags & kRowTokMember) != 0;
+                    const float lp = fmaf(sp.x_tok, a.c, -scaled_max(sp.m, a.c));  // log2 of the weights
+                    const float lq = fmaf(sq.x_tok, a.c, -scaled_max(sq.m, a.c));
+                    pp = pm ? ex2(lp) * sp.inv_zn : 0.0f;
+                    qq = qm ? ex2(lq) * sq.inv_zn : 0.0f;
+                    // q = 0 (the token outside q's nucleus) rejects; a weight
+                    // that only underflowed in fp32 takes the ratio from the
+                    // logits, differenced before scaling (the exponents
+                    // themselves are large and would lose digits)
+                    float ratio = 0.0f;
+                    if (pm && qm)
+                        ratio = (pp > 0.0f && qq > 0.0f)
+                                    ? pp / qq
+                                    : ex2(((sp.x_tok - sq.x_tok) - (sp.m - sq.m)) * a.c) * (sp.inv_zn / sq.inv_zn);
                     ap = fminf(1.0f, ratio);
                     acc = uniform01(a.seed, req, pos + i + 1, kPurposeAccept, 0) < ratio;
                 }

@@ -1,10 +1,35 @@
-// Host-side launch helpers: grid sizing against the SM count, opt-in to
-// large dynamic shared memory.
+// Host-side launch helpers: the caller's current device kept across a call,
+// grid sizing against the SM count, opt-in to large dynamic shared memory,
+// both cached per (device, kernel, shared memory, block).
 #pragma once
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 namespace sv {
+
+// Puts back, when the scope ends, the device that was current when it
+// began: the entry points make the logits' device current for their own
+// launches and must not leave the caller on another device.
+class DeviceGuard {
+  public:
+    DeviceGuard() {
+        ok_ = cudaGetDevice(&prev_) == cudaSuccess;
+        if (!ok_) cudaGetLastError();
+    }
+    ~DeviceGuard() {
+        if (!ok_) return;
+        int cur = -1;
+        if (cudaGetDevice(&cur) == cudaSuccess && cur != prev_) cudaSetDevice(prev_);
+    }
+    DeviceGuard(const DeviceGuard&) = delete;
+    DeviceGuard& operator=(const DeviceGuard&) = delete;
+
+  private:
+    int prev_ = 0;
+    bool ok_ = false;
+};
 
 // Make the device that owns `p` current for this library's CUDA runtime
 // (the runtime is linked statically, so its current device is its own).
@@ -18,17 +43,35 @@ inline bool select_device_of(const void* p) {
     return cudaSetDevice(at.device) == cudaSuccess;
 }
 
-inline int sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    return n;
-}
-
-// Persistent grid: min(work, SMs * resident CTAs per SM).  Sets the
-// kernel's dynamic shared-memory limit first.
-template <typename K>
-inline bool launch_grid(K kernel, size_t dyn_smem, long long work, int* grid, int block = 512) {
+// Resident CTAs per SM and SM count of a kernel launch configuration on the
+// current device, with the kernel's shared-memory attributes set.  The
+// first call per (device, kernel, dyn_smem, block) queries and sets; later
+// calls read the cache.
+struct LaunchShape {
+    int per_sm, sms;
+};
+inline bool launch_shape(const void* kernel, size_t dyn_smem, int block, LaunchShape* out) {
+    struct Entry {
+        const void* fn;
+        int dev;
+        size_t dyn;
+        int block;
+        LaunchShape shape;
+    };
+    constexpr int kEntries = 64;
+    static std::mutex mu;
+    static Entry table[kEntries];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (table[i].fn == kernel && table[i].dev == dev && table[i].dyn == dyn_smem && table[i].block == block) {
+                *out = table[i].shape;
+                return true;
+            }
+    }
     if (dyn_smem > 0 &&
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) != cudaSuccess)
         return false;
@@ -37,22 +80,35 @@ inline bool launch_grid(K kernel, size_t dyn_smem, long long work, int* grid, in
     if (dyn_smem >= 48 * 1024 &&
         cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
         return false;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block, dyn_smem) != cudaSuccess) return false;
-    const int sms = sm_count();
-    if (per_sm < 1 || sms < 1) return false;
-    long long g = (long long)sms * per_sm;
+    LaunchShape sh{0, 0};
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&sh.per_sm, kernel, block, dyn_smem) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&sh.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+    if (sh.per_sm < 1 || sh.sms < 1) return false;
+    std::lock_guard<std::mutex> lock(mu);
+    if (used < kEntries) table[used++] = Entry{kernel, dev, dyn_smem, block, sh};
+    *out = sh;
+    return true;
+}
+
+// Persistent grid: min(work, SMs * resident CTAs per SM).
+template <typename K>
+inline bool launch_grid(K kernel, size_t dyn_smem, long long work, int* grid, int block = 512) {
+    LaunchShape sh;
+    if (!launch_shape(reinterpret_cast<const void*>(kernel), dyn_smem, block, &sh)) return false;
+    long long g = (long long)sh.sms * sh.per_sm;
     if (work < g) g = work;
     *grid = (int)(g < 1 ? 1 : g);
     return true;
 }
 
-// Opt in to dyn_smem bytes of dynamic shared memory: static plus dynamic
-// above 48 KiB needs it even when the dynamic part alone is smaller.
+// Opt in to dyn_smem bytes of dynamic shared memory (static plus dynamic
+// above 48 KiB needs it even when the dynamic part alone is smaller); the
+// attribute is set once per (device, kernel, size).
 template <typename K>
-inline bool set_dyn_smem(K kernel, size_t dyn_smem) {
+inline bool set_dyn_smem(K kernel, size_t dyn_smem, int block) {
     if (dyn_smem == 0) return true;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn_smem) == cudaSuccess;
+    LaunchShape sh;
+    return launch_shape(reinterpret_cast<const void*>(kernel), dyn_smem, block, &sh);
 }
 
 }  // namespace sv

@@ -123,6 +123,7 @@ extern "C" spec_status spec_verify_linear(const void* target_logits, const void*
                                           int32_t* out_tokens, float* accept_prob, float* token_probs,
                                           int32_t* len_hist, int32_t* dev_error, void* workspace,
                                           size_t workspace_bytes, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
     if (!accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
     LinearArgs a;
     int mode = 0;
@@ -148,6 +149,7 @@ extern "C" spec_status spec_linear_stats(const void* target_logits, const void* 
                                          const int32_t* draft_tokens, int B, int k, int V,
                                          const spec_sampling_params* params, void* workspace, size_t workspace_bytes,
                                          spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
     LinearArgs a;
     int mode = 0;
     const spec_status r = prepare_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, nullptr, nullptr,
@@ -163,6 +165,7 @@ extern "C" spec_status spec_linear_decide(const void* target_logits, const void*
                                           int32_t* out_tokens, float* accept_prob, float* token_probs,
                                           int32_t* len_hist, int32_t* dev_error, const void* workspace,
                                           size_t workspace_bytes, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
     if (!accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
     LinearArgs a;
     int mode = 0;
@@ -231,6 +234,7 @@ extern "C" spec_status spec_verify_linear_noalloc(const void* target_logits, con
                                                   const spec_sampling_params* params, int32_t* accepted_len,
                                                   int32_t* out_tokens, float* accept_prob, float* token_probs,
                                                   int32_t* len_hist, int32_t* dev_error, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
     if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
     if ((int64_t)B * (2 * (int64_t)k + 1) > kNoAllocMaxRows) return SPEC_ERR_UNSUPPORTED;
     if (!target_logits || !select_device_of(target_logits)) return SPEC_ERR_INVALID_ARG;

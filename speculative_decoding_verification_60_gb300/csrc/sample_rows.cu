@@ -80,6 +80,7 @@ extern "C" spec_status spec_sample_rows(const void* logits, spec_dtype dtype, in
                                         const int64_t* request_ids, const int64_t* positions,
                                         const spec_sampling_params* params, int32_t* out_tokens,
                                         int32_t* dev_error, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
     if (!logits || !params || !out_tokens) return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
     if (R < 1 || V < 1) return SPEC_ERR_INVALID_ARG;

@@ -123,6 +123,11 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
             __syncthreads();
         }
         const int m = sh_m;
+        if (m > kMaxChildren) {  // every mode: a node with more children than the kernel tests
+            if (tid == 0) atomicOr(&sh_inval, kDevErrParent);
+            inval = true;
+            break;
+        }
         const T* prow = tgt + (size_t)n * V;
         const RowStat sp = row_stats<T, MODE>(prow, V, a.c, a.top_p, -1, topsmem, s, ss);
         if (sp.flags & kRowInvalid) {
@@ -158,11 +163,6 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
                 P.probs(i0, cnt, w);
             };
             t = block_inverse_cdf<VEC>(rv.units(), up, wp, s, ss);
-            break;
-        }
-        if (m > kMaxChildren) {
-            if (tid == 0) atomicOr(&sh_inval, kDevErrParent);
-            inval = true;
             break;
         }
         RowStat sq = sp;
@@ -260,7 +260,7 @@ template <typename T, int MODE>
 static spec_status launch_tree(TreeArgs& a, cudaStream_t st) {
     const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kTopSmemBytes : 0;
     auto* k = k_tree<T, MODE>;
-    if (!set_dyn_smem(k, dyn)) return SPEC_ERR_CUDA;
+    if (!set_dyn_smem(k, dyn, kNT)) return SPEC_ERR_CUDA;
     k<<<a.B, kNT, dyn, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
@@ -275,6 +275,7 @@ extern "C" spec_status spec_verify_tree(const void* target_logits, const void* d
                                         const spec_sampling_params* params, int32_t* accepted_len,
                                         int32_t* path_nodes, int32_t* out_tokens, int32_t* dev_error,
                                         void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
     if (!params || !target_logits || !node_tokens || !parent || !accepted_len || !path_nodes || !out_tokens)
         return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;

@@ -136,3 +136,34 @@ def test_ties_and_constant_rows():
         ref = oracle_linear(tgt, drf, d, T, top_p, 11, req, pos, range(B))
         compare_linear(got, ref, range(B), greedy=(T == 0.0), label=f"ties T={T} p={top_p}",
                        margin_of=lambda b, i: row_topp_margin(tgt, drf, b, i, T, top_p))
+
+
+@pytest.mark.parametrize("gap", [1.0, -1.0])
+def test_far_tail_draft_token_decides_like_the_oracle(gap):
+    """Caller-supplied drafts in the far tail of q: q(d) underflows in fp32
+    (about e^-250 of the row maximum) while p(d) / q(d) stays moderate (e^gap
+    times the normalisers' ratio).  The decision must follow the exact
+    ratio, as the fp64 oracle takes it ("Fast Inference from Transformers
+    via Speculative Decoding": accept with probability min(1, p/q))."""
+    B, k, V, T, top_p, seed = 8, 2, 256, 1.0, 1.0, 3
+    g = torch.Generator().manual_seed(41)
+    tgt = torch.randn(B, k + 1, V, generator=g)
+    drf = tgt[:, :k] + 0.3 * torch.randn(B, k, V, generator=g)
+    d = np.zeros((B, k), dtype=np.int32)
+    for b in range(B):
+        for i in range(k):
+            x = (b * 37 + i * 11) % V
+            d[b, i] = x
+            drf[b, i, x] = -250.0
+            tgt[b, i, x] = -250.0 + gap
+    tgt, drf = tgt.to(torch.bfloat16), drf.to(torch.bfloat16)
+    req = np.arange(B, dtype=np.int64) + 5
+    pos = np.arange(B, dtype=np.int64) * 2
+    got = run_gpu_linear(tgt, drf, d, T, top_p, seed, req, pos)
+    ref = oracle_linear(tgt, drf, d, T, top_p, seed, req, pos, range(B))
+    assert np.array_equal(got["accepted_len"], ref["accepted_len"])
+    assert np.array_equal(got["out_tokens"], ref["out_tokens"])
+    np.testing.assert_allclose(got["accept_prob"], ref["accept_prob"], rtol=1e-5, atol=1e-6)
+    if gap > 0:  # p/q > 1 on every drafted token: everything accepted
+        assert np.all(got["accepted_len"] == k)
+    assert int(got["dev_error"][0]) == 0

@@ -113,3 +113,23 @@ def test_bad_parent_and_tokens_are_flagged():
     bad_parent = np.array([-1, 0, 3, 1], dtype=np.int32)
     got = run_gpu_tree(tgt, drf, tok, bad_parent, 1.0, 1.0, 5, oracle.CHILD_IID, req, pos, max_depth=2)
     assert int(got["dev_error"][0]) & spec_bits(oracle.ERR_PARENT)
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_more_children_than_tested_is_flagged_in_every_mode(T):
+    """A node with 65 children (the kernel tests at most 64 per node) is
+    reported as a bad tree in greedy and sampled mode alike, and the request
+    takes the defined fallback (nothing accepted, the argmax of row 0)."""
+    B, V, N = 2, 128, 66
+    parent = np.array([-1] + [0] * (N - 1), dtype=np.int32)
+    tgt, drf = synth.tree_logits(B, N, V, 23)
+    tok = np.zeros((B, N), dtype=np.int32)
+    tok[:, 1:] = np.arange(N - 1) % V
+    tok[:, N - 1] = oracle.argmax(tgt[0, 0])  # greedy would accept the 65th child
+    req = np.arange(B, dtype=np.int64)
+    pos = np.zeros(B, dtype=np.int64)
+    got = run_gpu_tree(tgt, drf, tok, parent, T, 1.0, 7, oracle.CHILD_IID, req, pos)
+    assert int(got["dev_error"][0]) & spec_bits(oracle.ERR_PARENT)
+    for b in range(B):
+        assert got["accepted_len"][b] == 0
+        assert got["out_tokens"][b, 0] == oracle.argmax(tgt[b, 0])

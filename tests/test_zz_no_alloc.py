@@ -32,17 +32,20 @@ def _inputs(seed, B=12, k=4, V=5000, T=0.8):
     from gpu_parity import draft_tokens_from_oracle
 
     tgt, drf = synth.linear_logits(B, k, V, "bf16", data_seed=seed)
-    d = draft_tokens_from_oracle(drf, T, 0.9, seed=seed)
+    if B > 64:  # many requests: uniform drafts (the comparison is with the workspace call)
+        d = synth.uniform_tokens((B, k), V, seed).numpy()
+    else:
+        d = draft_tokens_from_oracle(drf, T if T > 0 else 1.0, 0.9, seed=seed)
     dev = torch.device("cuda:0")
     return (tgt.to(dev), drf.to(dev), torch.from_numpy(d).to(dev),
             torch.arange(B, dtype=torch.int64, device=dev) + 7, torch.full((B,), 40, dtype=torch.int64, device=dev))
 
 
-def _noalloc(svp, tgt, drf, d, req, pos, T, top_p, seed):
+def _noalloc(svp, tgt, drf, d, req, pos, T, top_p, seed, out=None):
     B, k1, V = tgt.shape
     k = k1 - 1
     dev = tgt.device
-    out = dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+    out = out or dict(accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
                out_tokens=torch.empty(B, k + 1, dtype=torch.int32, device=dev),
                accept_prob=torch.empty(B, k, dtype=torch.float32, device=dev),
                token_probs=torch.empty(B, k, 2, dtype=torch.float32, device=dev),
@@ -58,10 +61,14 @@ def _noalloc(svp, tgt, drf, d, req, pos, T, top_p, seed):
     return out
 
 
-def test_noalloc_matches_workspace_call_twice_in_a_row(lib):
+@pytest.mark.parametrize("B,k,V", [(12, 4, 5000), (21845, 1, 64)])
+def test_noalloc_matches_workspace_call_twice_in_a_row(lib, B, k, V):
+    """Sampled with top-p, sampled without it, and greedy, each called twice
+    on the same array; (21845, 1, 64) fills 65535 of its 65536 rows (no odd
+    row count reaches 65536 itself)."""
     svp = lib
-    for seed, (T, top_p) in ((21, (0.8, 0.9)), (22, (1.0, 1.0))):
-        tgt, drf, d, req, pos = _inputs(seed, T=T)
+    for seed, (T, top_p) in ((21, (0.8, 0.9)), (22, (1.0, 1.0)), (23, (0.0, 1.0))):
+        tgt, drf, d, req, pos = _inputs(seed, B=B, k=k, V=V, T=T)
         got = _noalloc(svp, tgt, drf, d, req, pos, T, top_p, seed)
         ref = svp.verify_linear(tgt, drf, d, T, top_p, seed, request_ids=req, positions=pos)
         torch.cuda.synchronize()
@@ -80,3 +87,18 @@ def test_noalloc_rejects_batches_above_its_limit(lib):
     st = svp.load().spec_verify_linear_noalloc(P, P, 0, P, 4096, 8, 8, None, None, ctypes.byref(sp), P, P,
                                                None, None, None, None, None)
     assert svp.status_string(st) == "SPEC_ERR_UNSUPPORTED"
+
+
+def test_noalloc_allocates_no_device_memory(lib):
+    """After a first call on the device (which looks up the array), further
+    calls leave the device's free memory as it was."""
+    svp = lib
+    tgt, drf, d, req, pos = _inputs(31, B=16, k=3, V=3000, T=0.9)
+    out = _noalloc(svp, tgt, drf, d, req, pos, 0.9, 0.9, 5)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        _noalloc(svp, tgt, drf, d, req, pos, 0.9, 0.9, 5, out=out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
