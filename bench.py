@@ -56,6 +56,7 @@ def parse_args():
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs on a smaller batch)")
     ap.add_argument("--no-tree", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 20 if args.impl == "reference" else 500
@@ -220,7 +221,7 @@ class LinearStep:
     """Device-resident inputs, outputs and workspace of one rank's batch,
     and the raw C-ABI calls of one step."""
 
-    def __init__(self, rank: int, device, batch=None):
+    def __init__(self, rank: int, device, batch=None, workload: str = WORKLOAD, temperature=None):
         import torch
 
         import speculative_decoding_verification_60_gb300 as svp
@@ -229,17 +230,22 @@ class LinearStep:
         self.torch = torch
         self.svp = svp
         self.lib = svp.load()
-        w = synth.WORKLOADS[WORKLOAD]
+        w = synth.WORKLOADS[workload]
+        self.workload = workload
         self.B, self.k, self.V = (batch or w["B"]), w["k"], w["V"]
-        self.T, self.top_p, self.seed = w["T"], w["top_p"], w["seed"]
+        self.T = w["T"] if temperature is None else temperature
+        self.top_p, self.seed = w["top_p"], w["seed"]
+        self.H = w.get("H", HIDDEN)
         B, k, V = self.B, self.k, self.V
         self.dev = device
         sh = shard(rank, B, w["data_seed"])
         self.tgt, self.drf = synth.linear_logits(B, k, V, "bf16", sh["data_seed"], device=device)
-        self.d = draft_tokens_torch(self.drf, self.T, self.top_p, seed=sh["draft_seed"])
+        # drafts: the draft model's own samples (greedy: its argmax)
+        self.d = (draft_tokens_torch(self.drf, self.T, self.top_p, seed=sh["draft_seed"]) if self.T > 0
+                  else self.drf.argmax(dim=-1).to(torch.int32))
         self.req = (torch.arange(B, dtype=torch.int64, device=device) + sh["first_request"])
         self.pos = torch.full((B,), 1000, dtype=torch.int64, device=device)
-        self.hidden = synth.hidden_states(B, k + 1, HIDDEN, seed=sh["hidden_seed"], device=device)
+        self.hidden = synth.hidden_states(B, k + 1, self.H, seed=sh["hidden_seed"], device=device)
         ws = svp.workspace_size(svp.SPEC_OP_LINEAR, B, k, V)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         i32, f32 = torch.int32, torch.float32
@@ -249,12 +255,17 @@ class LinearStep:
         self.tprob = torch.empty(B, k, 2, dtype=f32, device=device)
         self.hist = torch.empty(k + 1, dtype=i32, device=device)
         self.err = torch.empty(1, dtype=i32, device=device)
-        self.ohid = torch.empty(B * (k + 1), HIDDEN, dtype=torch.bfloat16, device=device)
+        self.ohid = torch.empty(B * (k + 1), self.H, dtype=torch.bfloat16, device=device)
         self.offs = torch.empty(B + 1, dtype=i32, device=device)
         self.ntok = torch.empty(B * (k + 1), dtype=i32, device=device)
         self.cerr = torch.empty(1, dtype=i32, device=device)
         self.sp = svp.SamplingParams(self.T, self.top_p, self.seed, 0)
-        self.algo_bytes = B * (2 * k + 1) * V * 2  # one read of every target and draft row
+        # one read of every target and draft row (greedy: target rows only)
+        self.algo_bytes = B * ((2 * k + 1) if self.T > 0 else (k + 1)) * V * 2
+        self.mode = 0 if self.T == 0 else (2 if self.top_p < 1.0 else 1)
+        # launches of one step: row statistics (one-read top-p pass, then the
+        # two-pass kernel on the rows it leaves), decisions, compaction
+        self.launches_per_step = (2 if self.mode == 2 else 1) + 2
 
     @staticmethod
     def P(t):
@@ -285,7 +296,7 @@ class LinearStep:
 
     def compact(self, stream):
         P = self.P
-        st = self.lib.spec_compact_accepted(P(self.hidden), self.B, self.k + 1, HIDDEN, P(self.acc), None,
+        st = self.lib.spec_compact_accepted(P(self.hidden), self.B, self.k + 1, self.H, P(self.acc), None,
                                             P(self.toks), self.k + 1, P(self.ohid), P(self.offs), P(self.ntok),
                                             P(self.cerr), ctypes.c_void_p(stream.cuda_stream))
         assert st == 0, self.svp.status_string(st)
@@ -317,7 +328,7 @@ def time_linear(step: LinearStep, K: int, W: int, barrier):
     barrier()
     ms = e0.elapsed_time(e1) / K
     stats_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    return ms, stats_ms, 3 * K
+    return ms, stats_ms, step.launches_per_step * K
 
 
 def time_e2e(step: LinearStep, K: int, chunks: int = 4):
@@ -344,6 +355,8 @@ def time_e2e(step: LinearStep, K: int, chunks: int = 4):
                      device=step.dev)
     hist = torch.empty(chunks, k + 1, dtype=torch.int32, device=step.dev)
     offs = torch.empty(chunks, Bc + 1, dtype=torch.int32, device=step.dev)
+    errs = torch.zeros(chunks, dtype=torch.int32, device=step.dev)  # one slot per group: each call zeroes its own
+    cerrs = torch.zeros(chunks, dtype=torch.int32, device=step.dev)
 
     def one():
         ready = []
@@ -362,12 +375,12 @@ def time_e2e(step: LinearStep, K: int, chunks: int = 4):
             st = step.lib.spec_verify_linear(
                 P(step.tgt[lo:hi]), P(step.drf[lo:hi]), 0, P(step.d[lo:hi]), n, k, V, P(step.req[lo:hi]),
                 P(step.pos[lo:hi]), ctypes.byref(step.sp), P(step.acc[lo:hi]), P(step.toks[lo:hi]),
-                P(step.aprob[lo:hi]), P(step.tprob[lo:hi]), P(hist[c]), P(step.err), P(ws), ws.numel(),
+                P(step.aprob[lo:hi]), P(step.tprob[lo:hi]), P(hist[c]), P(errs[c:c + 1]), P(ws), ws.numel(),
                 ctypes.c_void_p(comp.cuda_stream))
             assert st == 0, step.svp.status_string(st)
             st = step.lib.spec_compact_accepted(
-                P(step.hidden[lo:hi]), n, k + 1, HIDDEN, P(step.acc[lo:hi]), None, P(step.toks[lo:hi]), k + 1,
-                P(step.ohid[lo * (k + 1):]), P(offs[c]), P(step.ntok[lo * (k + 1):]), P(step.cerr),
+                P(step.hidden[lo:hi]), n, k + 1, step.H, P(step.acc[lo:hi]), None, P(step.toks[lo:hi]), k + 1,
+                P(step.ohid[lo * (k + 1):]), P(offs[c]), P(step.ntok[lo * (k + 1):]), P(cerrs[c:c + 1]),
                 ctypes.c_void_p(comp.cuda_stream))
             assert st == 0, step.svp.status_string(st)
             for o, oh in zip(outs, outs_h):
@@ -383,7 +396,10 @@ def time_e2e(step: LinearStep, K: int, chunks: int = 4):
     comp.wait_stream(copy)
     e1.record(comp)
     torch.cuda.synchronize()
-    return e0.elapsed_time(e1) / K, h2d, d2h, chunks
+    err = 0
+    for v in torch.cat([errs, cerrs]).tolist():  # device errors of the last step, every group
+        err |= int(v)
+    return e0.elapsed_time(e1) / K, h2d, d2h, chunks, err
 
 
 def time_sampler(step: LinearStep, K: int, W: int, peak: float):
@@ -418,7 +434,10 @@ def time_sampler(step: LinearStep, K: int, W: int, peak: float):
             "launches": K, "l2": "flushed before every launch"}
 
 
-def time_tree(device, K: int, W: int):
+def time_tree(device, K: int, W: int, peak: float):
+    """The tree workload (B=32, 60-node top-4 tree of depth 5): each node's
+    children are distinct tokens drawn without replacement from the
+    parent's draft row (input generation only), verified in WOR mode."""
     import numpy as np
     import torch
 
@@ -429,50 +448,147 @@ def time_tree(device, K: int, W: int):
     B, N, V = w["B"], w["N"], w["V"]
     parent = synth.pruned_tree(w["K"], w["depth"], N)
     tgt, drf = synth.tree_logits(B, N, V, w["data_seed"], device=device)
-    # node tokens: each child drawn from its parent's draft row (input generation only)
     tok = torch.zeros(B, N, dtype=torch.int32, device=device)
-    par = torch.as_tensor(parent, dtype=torch.long, device=device)
-    flat = drf[:, par[1:]].reshape(B * (N - 1), V).float() / w["T"]
     g = torch.Generator(device=device)
     g.manual_seed(w["data_seed"] + 5)
-    tok[:, 1:] = torch.multinomial(torch.softmax(flat, -1), 1, generator=g).reshape(B, N - 1).to(torch.int32)
+    for n in range(N):
+        kids = [i for i in range(1, N) if parent[i] == n]
+        if kids:
+            p = torch.softmax(drf[:, n].float() / w["T"], -1)
+            tok[:, kids] = torch.multinomial(p, len(kids), replacement=False, generator=g).to(torch.int32)
     parent_d = torch.as_tensor(parent, dtype=torch.int32, device=device)
     out = None
     for _ in range(W):
-        out = svp.verify_tree(tgt, drf, tok, parent_d, w["depth"], w["T"], w["top_p"], w["seed"], svp.CHILD_IID)
+        out = svp.verify_tree(tgt, drf, tok, parent_d, w["depth"], w["T"], w["top_p"], w["seed"], svp.CHILD_WOR)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for _ in range(K):
-        out = svp.verify_tree(tgt, drf, tok, parent_d, w["depth"], w["T"], w["top_p"], w["seed"], svp.CHILD_IID)
+        out = svp.verify_tree(tgt, drf, tok, parent_d, w["depth"], w["T"], w["top_p"], w["seed"], svp.CHILD_WOR)
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / K
     acc = out["accepted_len"].cpu().numpy()
-    return {"workload": TREE_WORKLOAD, "ms_per_step": round(ms, 4), "requests": B,
-            "verified_nodes_per_s": round(B * N / (ms / 1e3), 1), "mean_accepted_depth": float(np.mean(acc)),
-            "child_mode": "iid"}
+    visited = int(np.sum(acc + 1))                # nodes on the accepted paths (each a target and a draft row)
+    path_bytes = visited * 2 * V * 2
+    all_bytes = B * N * 2 * V * 2
+    gbps = path_bytes / (ms / 1e3) / 1e9
+    return {"workload": TREE_WORKLOAD, "ms_per_step": round(ms, 4), "requests": B, "child_mode": "wor",
+            "children": "distinct tokens drawn without replacement from the parent's draft row",
+            "visited_nodes": visited, "visited_nodes_per_s": round(visited / (ms / 1e3), 1),
+            "mean_accepted_depth": float(np.mean(acc)), "path_bytes": path_bytes, "all_nodes_bytes": all_bytes,
+            "path_gbps": round(gbps, 1), "frac": round(gbps / peak, 4)}
+
+
+# The other workloads the method's pages describe, timed beside the headline
+# one: a Llama-1B draft for a 70B-class target (B=64, k=4, T=1) and
+# DeepSeek-scale MTP verification with the 7168-wide hidden-state gather
+# (B=1024, k=3, V=129280), sampled and greedy.
+EXTRA_WORKLOADS = (("linear-b64-k4-v128256", None), ("linear-b1024-k3-v129280-h7168", None),
+                   ("linear-b1024-k3-v129280-h7168", 0.0))
+
+
+def time_workload(name: str, temperature, rank: int, world: int, device, K: int, W: int, peak: float, barrier):
+    """One extra workload: the same step (row statistics, decisions,
+    compaction) timed on its own inputs (larger than L2), with the row
+    statistics launch timed alone and the compaction's gather bytes."""
+    import torch
+
+    step = LinearStep(rank, device, workload=name, temperature=temperature)
+    ms, stats_ms, launches = time_linear(step, K, W, barrier)
+    ms, stats_ms = max_over_ranks([ms, stats_ms], world, device)
+    acc = step.acc.to(torch.int64)
+    gather = int(((acc + 1) * step.H * 2 * 2).sum())  # accepted hidden rows read and written
+    stats_gbps = step.algo_bytes / (stats_ms / 1e3) / 1e9
+    out = {"workload": name, "temperature": step.T, "top_p": step.top_p, "B": step.B, "k": step.k, "V": step.V,
+           "ms_per_step": round(ms, 4), "rows_per_s": round(job_value(step.B * (step.k + 1), world, ms), 1),
+           "stats_ms": round(stats_ms, 4), "stats_gbps": round(stats_gbps, 1), "frac": round(stats_gbps / peak, 4),
+           "step_bytes": step.algo_bytes + gather,
+           "step_gbps": round((step.algo_bytes + gather) / (ms / 1e3) / 1e9, 1),
+           "mean_accepted_len": round(float(acc.float().mean()), 4), "launches_per_step": launches // K,
+           "steps": K}
+    del step
+    torch.cuda.empty_cache()
+    return out
+
+
+def _oracle_request(job):
+    """One request through the oracle (a worker process of the all-cores
+    timing): returns its wall time."""
+    import oracle
+
+    tgt, drf, d, T, top_p, seed, req, pos = job
+    t0 = time.perf_counter()
+    oracle.verify_linear(tgt, drf, d, T, top_p, seed, req_ids=req, positions=pos)
+    return time.perf_counter() - t0
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
 
 
 def cpu_baseline(step: LinearStep, n_req: int) -> dict:
-    """The oracle, as it stands, on a bounded sample (n_req requests) of the
-    same batch, single-threaded on the host."""
+    """The oracle, as it stands, on bounded samples of the same batch: n_req
+    requests single-threaded (its results compared with the GPU's for the
+    same requests), then 2 requests per host core spread over every core
+    (one process per core)."""
+    import multiprocessing
+    from concurrent.futures import ProcessPoolExecutor
+
+    import numpy as np
+
     import oracle
 
-    sel = list(range(n_req))
+    sel = list(range(min(n_req, step.B)))
     tgt = step.tgt[sel].cpu()
     drf = step.drf[sel].cpu()
     d = step.d[sel].cpu().numpy()
     req = step.req[sel].cpu().numpy()
     pos = step.pos[sel].cpu().numpy()
+    g_acc = step.acc[sel].cpu().numpy()
+    g_tok = step.toks[sel].cpu().numpy()
+    g_tp = step.tprob[sel].cpu().numpy().astype(np.float64)
+    mism = excused = 0
+    perr = 0.0
     t0 = time.perf_counter()
-    for b in range(n_req):  # one request at a time, as the method defines it
-        oracle.verify_linear(tgt[b:b + 1], drf[b:b + 1], d[b:b + 1], step.T, step.top_p, step.seed,
-                             req_ids=req[b:b + 1], positions=pos[b:b + 1])
+    for j, b in enumerate(sel):  # one request at a time, as the method defines it
+        r = oracle.verify_linear(tgt[j:j + 1], drf[j:j + 1], d[j:j + 1], step.T, step.top_p, step.seed,
+                                 req_ids=req[j:j + 1], positions=pos[j:j + 1])
+        if int(r["accepted_len"][0]) != int(g_acc[j]) or not np.array_equal(r["out_tokens"][0], g_tok[j]):
+            if r["margin"][0] < 1e-6:
+                excused += 1
+            else:
+                mism += 1
+        perr = max(perr, float(np.max(np.abs(g_tp[j] - r["tok_p"][0]))))
     dt = time.perf_counter() - t0
-    return {"value": round(n_req * (step.k + 1) / dt, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{n_req} of {step.B} requests of {WORKLOAD} ({n_req * (2 * step.k + 1)} rows), "
-                      f"fp64 C oracle, {dt:.1f} s"}
+    single = {"value": round(len(sel) * (step.k + 1) / dt, 3), "cores": 1,
+              "sample": f"{len(sel)} of {step.B} requests of {step.workload} ({len(sel) * (2 * step.k + 1)} rows), "
+                        f"fp64 C oracle, {dt:.1f} s"}
+    cores = host_cores()
+    n_all = min(step.B, 2 * cores)
+    tf = step.tgt[:n_all].float().cpu().numpy()
+    qf = step.drf[:n_all].float().cpu().numpy()
+    dd = step.d[:n_all].cpu().numpy()
+    rq = step.req[:n_all].cpu().numpy()
+    ps = step.pos[:n_all].cpu().numpy()
+    jobs = [(tf[b:b + 1], qf[b:b + 1], dd[b:b + 1], step.T, step.top_p, step.seed, rq[b:b + 1], ps[b:b + 1])
+            for b in range(n_all)]
+    # spawn: this process already holds a CUDA context
+    with ProcessPoolExecutor(max_workers=cores, mp_context=multiprocessing.get_context("spawn")) as ex:
+        list(ex.map(_oracle_request, jobs[:cores]))  # start every worker (imports, library load)
+        t1 = time.perf_counter()
+        list(ex.map(_oracle_request, jobs))
+        wall = time.perf_counter() - t1
+    return {"value": round(n_all * (step.k + 1) / wall, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_all} of {step.B} requests of {step.workload}, one process per host core "
+                      f"({cores}), fp64 C oracle, {wall:.1f} s wall",
+            "single_core": single,
+            "parity": {"requests": len(sel), "mismatches": mism, "margin_excused": excused,
+                       "max_token_prob_err": perr, "bar": "identical a and tokens unless the oracle's decision "
+                                                         "margin is < 1e-6; token probabilities within 1e-5"}}
 
 
 def run_ours(args):
@@ -499,10 +615,13 @@ def run_ours(args):
     ms, stats_ms = max_over_ranks([ms, stats_ms], world, device)
     rows = step.B * (step.k + 1)
     value = job_value(rows, world, ms)
-    e2e_ms, h2d, d2h, chunks = (ms, 0, 0, 1) if args.no_e2e else time_e2e(step, args.e2e_steps)
+    e2e_ms, h2d, d2h, chunks, e2e_err = (ms, 0, 0, 1, 0) if args.no_e2e else time_e2e(step, args.e2e_steps)
     e2e_ms = max_over_ranks([e2e_ms], world, device)[0]
-    tree = None if args.no_tree else time_tree(device, max(3, args.steps // 2), 2)
     peak0, _ = hbm_peak()
+    tree = None if args.no_tree else time_tree(device, max(3, args.steps // 2), 2, peak0)
+    extra = [] if args.no_extra else [
+        time_workload(name, temp, rank, world, device, max(10, min(100, args.steps // 5)), 3, peak0, barrier)
+        for name, temp in EXTRA_WORKLOADS]
     sampler = time_sampler(step, max(3, min(50, args.steps)), 3, peak0)
     peak, peak_kind = hbm_peak()
     achieved = step.algo_bytes / (stats_ms / 1e3) / 1e9
@@ -530,12 +649,14 @@ def run_ours(args):
                      "algorithmic_bytes_per_launch": step.algo_bytes, "launch_ms": round(stats_ms, 4)},
         "e2e": {"value": round(job_value(rows, world, e2e_ms), 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipeline": f"{chunks} request groups, copy of group i+1 overlapping verification of group i"},
+                "pipeline": f"{chunks} request groups, copy of group i+1 overlapping verification of group i",
+                "dev_error": e2e_err},
         "gpu_launches": launches,
         "clocks": clk,
         "mean_accepted_len": round(float(acc.float().mean()), 4),
         "tree": tree,
         "draft_sampler": sampler,
+        "workloads": extra,
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(step, args.cpu_requests)
