@@ -258,47 +258,36 @@ class LinearStep:
         self.ohid = torch.empty(B * (k + 1), self.H, dtype=torch.bfloat16, device=device)
         self.offs = torch.empty(B + 1, dtype=i32, device=device)
         self.ntok = torch.empty(B * (k + 1), dtype=i32, device=device)
-        self.cerr = torch.empty(1, dtype=i32, device=device)
         self.sp = svp.SamplingParams(self.T, self.top_p, self.seed, 0)
         # one read of every target and draft row (greedy: target rows only)
         self.algo_bytes = B * ((2 * k + 1) if self.T > 0 else (k + 1)) * V * 2
         self.mode = 0 if self.T == 0 else (2 if self.top_p < 1.0 else 1)
         # launches of one step: row statistics (one-read top-p pass, then the
-        # two-pass kernel on the rows it leaves), decisions, compaction
-        self.launches_per_step = (2 if self.mode == 2 else 1) + 2
+        # two-pass kernel on the rows it leaves, whose last CTA takes the
+        # decisions), then the draw with the compaction
+        self.launches_per_step = (2 if self.mode == 2 else 1) + 1
 
     @staticmethod
     def P(t):
         return ctypes.c_void_p(t.data_ptr())
 
     def stats(self, stream):
+        """Row statistics with every request's accept decisions and packed offsets."""
         P = self.P
-        st = self.lib.spec_linear_stats(P(self.tgt), P(self.drf), 0, P(self.d), self.B, self.k, self.V,
-                                        ctypes.byref(self.sp), P(self.ws), self.ws.numel(),
-                                        ctypes.c_void_p(stream.cuda_stream))
+        st = self.lib.spec_linear_stats_decide(P(self.tgt), P(self.drf), 0, P(self.d), self.B, self.k, self.V,
+                                               P(self.req), P(self.pos), ctypes.byref(self.sp), P(self.acc),
+                                               P(self.aprob), P(self.tprob), P(self.hist), P(self.err), P(self.ws),
+                                               self.ws.numel(), ctypes.c_void_p(stream.cuda_stream))
         assert st == 0, self.svp.status_string(st)
 
-    def decide(self, stream):
+    def draw_compact(self, stream):
+        """The residual / bonus draw, with the accepted hidden rows and next
+        tokens packed for the next draft step in the same launch."""
         P = self.P
-        st = self.lib.spec_linear_decide(P(self.tgt), P(self.drf), 0, P(self.d), self.B, self.k, self.V, P(self.req),
-                                         P(self.pos), ctypes.byref(self.sp), P(self.acc), P(self.toks), P(self.aprob),
-                                         P(self.tprob), P(self.hist), P(self.err), P(self.ws), self.ws.numel(),
-                                         ctypes.c_void_p(stream.cuda_stream))
-        assert st == 0, self.svp.status_string(st)
-
-    def verify(self, stream):
-        P = self.P
-        st = self.lib.spec_verify_linear(P(self.tgt), P(self.drf), 0, P(self.d), self.B, self.k, self.V, P(self.req),
-                                         P(self.pos), ctypes.byref(self.sp), P(self.acc), P(self.toks), P(self.aprob),
-                                         P(self.tprob), P(self.hist), P(self.err), P(self.ws), self.ws.numel(),
-                                         ctypes.c_void_p(stream.cuda_stream))
-        assert st == 0, self.svp.status_string(st)
-
-    def compact(self, stream):
-        P = self.P
-        st = self.lib.spec_compact_accepted(P(self.hidden), self.B, self.k + 1, self.H, P(self.acc), None,
-                                            P(self.toks), self.k + 1, P(self.ohid), P(self.offs), P(self.ntok),
-                                            P(self.cerr), ctypes.c_void_p(stream.cuda_stream))
+        st = self.lib.spec_linear_draw(P(self.tgt), P(self.drf), 0, P(self.d), self.B, self.k, self.V, P(self.req),
+                                       P(self.pos), ctypes.byref(self.sp), P(self.hidden), self.H, P(self.toks),
+                                       P(self.ohid), P(self.offs), P(self.ntok), P(self.ws), self.ws.numel(),
+                                       ctypes.c_void_p(stream.cuda_stream))
         assert st == 0, self.svp.status_string(st)
 
 
@@ -309,8 +298,7 @@ def time_linear(step: LinearStep, K: int, W: int, barrier):
     s = torch.cuda.current_stream()
     for _ in range(W):
         step.stats(s)
-        step.decide(s)
-        step.compact(s)
+        step.draw_compact(s)
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
@@ -321,8 +309,7 @@ def time_linear(step: LinearStep, K: int, W: int, barrier):
         ev[i][0].record(s)
         step.stats(s)
         ev[i][1].record(s)
-        step.decide(s)
-        step.compact(s)
+        step.draw_compact(s)
     e1.record(s)
     torch.cuda.synchronize()
     barrier()
@@ -356,7 +343,6 @@ def time_e2e(step: LinearStep, K: int, chunks: int = 4):
     hist = torch.empty(chunks, k + 1, dtype=torch.int32, device=step.dev)
     offs = torch.empty(chunks, Bc + 1, dtype=torch.int32, device=step.dev)
     errs = torch.zeros(chunks, dtype=torch.int32, device=step.dev)  # one slot per group: each call zeroes its own
-    cerrs = torch.zeros(chunks, dtype=torch.int32, device=step.dev)
 
     def one():
         ready = []
@@ -372,16 +358,12 @@ def time_e2e(step: LinearStep, K: int, chunks: int = 4):
             lo, hi = c * Bc, min(B, (c + 1) * Bc)
             n = hi - lo
             comp.wait_event(ready[c])
-            st = step.lib.spec_verify_linear(
+            st = step.lib.spec_verify_linear_compact(
                 P(step.tgt[lo:hi]), P(step.drf[lo:hi]), 0, P(step.d[lo:hi]), n, k, V, P(step.req[lo:hi]),
-                P(step.pos[lo:hi]), ctypes.byref(step.sp), P(step.acc[lo:hi]), P(step.toks[lo:hi]),
-                P(step.aprob[lo:hi]), P(step.tprob[lo:hi]), P(hist[c]), P(errs[c:c + 1]), P(ws), ws.numel(),
-                ctypes.c_void_p(comp.cuda_stream))
-            assert st == 0, step.svp.status_string(st)
-            st = step.lib.spec_compact_accepted(
-                P(step.hidden[lo:hi]), n, k + 1, step.H, P(step.acc[lo:hi]), None, P(step.toks[lo:hi]), k + 1,
-                P(step.ohid[lo * (k + 1):]), P(offs[c]), P(step.ntok[lo * (k + 1):]), P(cerrs[c:c + 1]),
-                ctypes.c_void_p(comp.cuda_stream))
+                P(step.pos[lo:hi]), ctypes.byref(step.sp), P(step.hidden[lo:hi]), step.H, P(step.acc[lo:hi]),
+                P(step.toks[lo:hi]), P(step.aprob[lo:hi]), P(step.tprob[lo:hi]), P(hist[c]),
+                P(step.ohid[lo * (k + 1):]), P(offs[c]), P(step.ntok[lo * (k + 1):]), P(errs[c:c + 1]), P(ws),
+                ws.numel(), ctypes.c_void_p(comp.cuda_stream))
             assert st == 0, step.svp.status_string(st)
             for o, oh in zip(outs, outs_h):
                 oh[lo:hi].copy_(o[lo:hi], non_blocking=True)
@@ -397,7 +379,7 @@ def time_e2e(step: LinearStep, K: int, chunks: int = 4):
     e1.record(comp)
     torch.cuda.synchronize()
     err = 0
-    for v in torch.cat([errs, cerrs]).tolist():  # device errors of the last step, every group
+    for v in errs.tolist():  # device errors of the last step, every group
         err |= int(v)
     return e0.elapsed_time(e1) / K, h2d, d2h, chunks, err
 

@@ -157,26 +157,65 @@ spec_status spec_verify_linear(const void* target_logits, const void* draft_logi
                                void* workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /*
- * The two stages of spec_verify_linear, for callers that want to start the
- * streaming pass as soon as the logits exist or to time it on its own:
- * spec_linear_stats reads every target row (and every draft row when
- * T > 0) once and writes per-row statistics into `workspace`;
- * spec_linear_decide reads them back, runs the accept tests and the
- * residual / bonus draw, and writes the outputs.  Called in that order on
- * one stream with identical inputs, params and workspace, they give exactly
- * the results of spec_verify_linear (which is these two calls).  The
- * workspace must not be reused between them.  Arguments as above.
+ * Linear verification followed by the compaction of the accepted positions
+ * for the next draft step, in the same launches (section "MTP": token
+ * t_{i+1} is drawn from logits computed from hidden state H_i; section "MTP
+ * schedule for a single token": a kernel inserts the next target tokens,
+ * with no host synchronisation).  Results as spec_verify_linear followed by
+ * spec_compact_accepted(hidden, B, k+1, H, accepted_len, NULL, out_tokens,
+ * k+1, out_hidden, offsets, next_tokens, ...), without the compaction's own
+ * launch: the last CTA of the row-statistics launch takes every request's
+ * decisions and the packed offsets, and each request's draw CTA copies its
+ * a_b + 1 hidden rows and writes their next tokens.
+ *
+ *  hidden       [B, k+1, H] bf16 (2-byte elements, copied bit for bit):
+ *               row i is the hidden state after the prefix plus d_1..d_i.
+ *  out_hidden   [B*(k+1), H] out: row offsets[b] + r = hidden[b, r, :],
+ *               r = 0..a_b (rows past offsets[B] untouched).
+ *  offsets      [B+1] out: offsets[0] = 0, offsets[b+1] = offsets[b] + a_b + 1.
+ *  next_tokens  [B*(k+1)] out: next_tokens[offsets[b] + r] = out_tokens[b, r].
+ *  An invalid request (see spec_verify_linear) contributes its row 0 and
+ *  its fallback token.  Other arguments, outputs, limits and workspace as
+ *  spec_verify_linear; the vector path wants H * 2 a multiple of 16 and
+ *  16-byte aligned hidden pointers (else 2-byte copies).  B * (k+1) < 2^31.
  */
-spec_status spec_linear_stats(const void* target_logits, const void* draft_logits, spec_dtype dtype,
-                              const int32_t* draft_tokens, int B, int k, int V,
-                              const spec_sampling_params* params, void* workspace, size_t workspace_bytes,
-                              spec_stream_t stream);
-spec_status spec_linear_decide(const void* target_logits, const void* draft_logits, spec_dtype dtype,
-                               const int32_t* draft_tokens, int B, int k, int V,
-                               const int64_t* request_ids, const int64_t* positions,
-                               const spec_sampling_params* params, int32_t* accepted_len, int32_t* out_tokens,
-                               float* accept_prob, float* token_probs, int32_t* len_hist, int32_t* dev_error,
-                               const void* workspace, size_t workspace_bytes, spec_stream_t stream);
+spec_status spec_verify_linear_compact(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                       const int32_t* draft_tokens, int B, int k, int V,
+                                       const int64_t* request_ids, const int64_t* positions,
+                                       const spec_sampling_params* params, const void* hidden, int H,
+                                       int32_t* accepted_len, int32_t* out_tokens, float* accept_prob,
+                                       float* token_probs, int32_t* len_hist, void* out_hidden, int32_t* offsets,
+                                       int32_t* next_tokens, int32_t* dev_error, void* workspace,
+                                       size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * The two launch groups of spec_verify_linear (and of
+ * spec_verify_linear_compact), for callers that want to time them apart or
+ * start the streaming pass as soon as the logits exist.
+ * spec_linear_stats_decide reads every target row (and every draft row when
+ * T > 0) once, writes per-row statistics into `workspace`, and in the last
+ * CTA of that launch runs every request's accept tests: it writes
+ * accepted_len, accept_prob, token_probs, len_hist and dev_error (zeroing
+ * len_hist and dev_error first) and keeps each request's decision and the
+ * packed offsets in the workspace.  spec_linear_draw then draws every
+ * request's t* and writes out_tokens and, when hidden is not NULL, the
+ * compaction outputs of spec_verify_linear_compact (hidden NULL: H,
+ * out_hidden, offsets and next_tokens are ignored).  Called in that order
+ * on one stream with identical inputs, params and workspace, they give
+ * exactly the results of the one-call forms (which are these two calls).
+ * The workspace must not be reused between them.  Arguments as above.
+ */
+spec_status spec_linear_stats_decide(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                     const int32_t* draft_tokens, int B, int k, int V,
+                                     const int64_t* request_ids, const int64_t* positions,
+                                     const spec_sampling_params* params, int32_t* accepted_len, float* accept_prob,
+                                     float* token_probs, int32_t* len_hist, int32_t* dev_error, void* workspace,
+                                     size_t workspace_bytes, spec_stream_t stream);
+spec_status spec_linear_draw(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                             const int32_t* draft_tokens, int B, int k, int V, const int64_t* request_ids,
+                             const int64_t* positions, const spec_sampling_params* params, const void* hidden, int H,
+                             int32_t* out_tokens, void* out_hidden, int32_t* offsets, int32_t* next_tokens,
+                             const void* workspace, size_t workspace_bytes, spec_stream_t stream);
 
 /*
  * spec_verify_linear for callers that cannot allocate device memory at the
@@ -186,15 +225,16 @@ spec_status spec_linear_decide(const void* target_logits, const void* draft_logi
  * exists for those callers only.
  *
  * Same arguments and results as spec_verify_linear, without the workspace:
- * the per-row statistics go to a fixed 2 MiB array inside the library's
- * device image, which every GPU that loads the library keeps until the
- * process exits.  Limits: B * (2k + 1) <= 65536 rows, else
+ * the workspace (per-row statistics, decisions, offsets, a counter) lives in
+ * a fixed array of about 2.3 MiB inside the library's device image, which
+ * every GPU that loads the library keeps until the process exits.  Limits: B * (2k + 1) <= 65536 rows, else
  * SPEC_ERR_UNSUPPORTED (nothing is enqueued).  The call allocates nothing
  * (no cudaMalloc, cudaFree or allocating library routine).  The first call
  * on each device looks up the array's device address once; make that first
  * call before any stream capture.  Every call shares the one array, so
  * calls that overlap on the GPU (different streams or host threads) race on
- * it; each call writes every row it later reads, so no state carries over.
+ * it; each call clears the counter and writes every record it later reads,
+ * so no state carries over.
  */
 spec_status spec_verify_linear_noalloc(const void* target_logits, const void* draft_logits, spec_dtype dtype,
                                        const int32_t* draft_tokens, int B, int k, int V,

@@ -24,6 +24,7 @@ from ._binding import (  # noqa: F401
     sample_rows,
     status_string,
     verify_linear,
+    verify_linear_compact,
     verify_tree,
     workspace_size,
 )

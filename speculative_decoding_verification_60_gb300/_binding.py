@@ -23,9 +23,9 @@ CHILD_WOR, CHILD_IID, CHILD_DETERMINISTIC = 0, 1, 2
 DEVERR_TOKEN, DEVERR_NONFINITE, DEVERR_PARENT, DEVERR_LENGTH = 1, 2, 4, 8
 
 # Every symbol declared in include/specverify.h.
-EXPORTS = ("spec_workspace_size", "spec_verify_linear", "spec_linear_stats", "spec_linear_decide",
-           "spec_verify_linear_noalloc", "spec_verify_tree", "spec_compact_accepted", "spec_sample_rows",
-           "spec_status_string")
+EXPORTS = ("spec_workspace_size", "spec_verify_linear", "spec_verify_linear_compact", "spec_linear_stats_decide",
+           "spec_linear_draw", "spec_verify_linear_noalloc", "spec_verify_tree", "spec_compact_accepted",
+           "spec_sample_rows", "spec_status_string")
 
 
 class SamplingParams(ctypes.Structure):
@@ -57,11 +57,15 @@ def load() -> ctypes.CDLL:
     lib.spec_verify_linear.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams),
                                        P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_linear.restype = I
-    lib.spec_linear_stats.argtypes = [P, P, I, P, I, I, I, ctypes.POINTER(SamplingParams), P, Z, P]
-    lib.spec_linear_stats.restype = I
-    lib.spec_linear_decide.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams),
-                                       P, P, P, P, P, P, P, Z, P]
-    lib.spec_linear_decide.restype = I
+    lib.spec_verify_linear_compact.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams), P, I,
+                                               P, P, P, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_linear_compact.restype = I
+    lib.spec_linear_stats_decide.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams),
+                                             P, P, P, P, P, P, Z, P]
+    lib.spec_linear_stats_decide.restype = I
+    lib.spec_linear_draw.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams), P, I,
+                                     P, P, P, P, P, Z, P]
+    lib.spec_linear_draw.restype = I
     lib.spec_verify_linear_noalloc.argtypes = [P, P, I, P, I, I, I, P, P, ctypes.POINTER(SamplingParams),
                                                P, P, P, P, P, P, P]
     lib.spec_verify_linear_noalloc.restype = I
@@ -156,6 +160,49 @@ def verify_linear(target, draft, draft_tokens, temperature: float, top_p: float 
                                 _ptr(out.get("dev_error")), _ptr(workspace), workspace.numel(), _stream(stream))
     if st != SPEC_OK:
         raise SpecError("spec_verify_linear", st)
+    return out
+
+
+def verify_linear_compact(target, draft, draft_tokens, hidden, temperature: float, top_p: float = 1.0,
+                          seed: int = 0, request_ids=None, positions=None, stream=None) -> dict:
+    """``spec_verify_linear_compact`` on torch tensors: verify_linear plus
+    hidden [B, k+1, H] bf16; the dict adds out_hidden [B*(k+1), H],
+    offsets [B+1] and next_tokens [B*(k+1)] (rows past offsets[B] are not
+    written)."""
+    lib = load()
+    B, k1, V = target.shape
+    k = k1 - 1
+    H = hidden.shape[-1]
+    dt = _dtype_code(target)
+    _check(target, "target")
+    _check(draft, "draft", target.dtype, (B, k, V))
+    _check(draft_tokens, "draft_tokens", torch.int32, (B, k))
+    _check(hidden, "hidden", torch.bfloat16, (B, k + 1, H))
+    _check(request_ids, "request_ids", torch.int64, (B,))
+    _check(positions, "positions", torch.int64, (B,))
+    dev = target.device
+    out = dict(
+        accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+        out_tokens=torch.empty(B, k + 1, dtype=torch.int32, device=dev),
+        accept_prob=torch.empty(B, k, dtype=torch.float32, device=dev),
+        token_probs=torch.empty(B, k, 2, dtype=torch.float32, device=dev),
+        len_hist=torch.empty(k + 1, dtype=torch.int32, device=dev),
+        out_hidden=torch.zeros(B * (k + 1), H, dtype=torch.bfloat16, device=dev),
+        offsets=torch.empty(B + 1, dtype=torch.int32, device=dev),
+        next_tokens=torch.full((B * (k + 1),), -1, dtype=torch.int32, device=dev),
+        dev_error=torch.empty(1, dtype=torch.int32, device=dev),
+    )
+    need = workspace_size(SPEC_OP_LINEAR, B, k, V, dt)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    sp = SamplingParams(float(temperature), float(top_p), int(seed) & (2**64 - 1), 0)
+    st = lib.spec_verify_linear_compact(_ptr(target), _ptr(draft), dt, _ptr(draft_tokens), B, k, V,
+                                        _ptr(request_ids), _ptr(positions), ctypes.byref(sp), _ptr(hidden), H,
+                                        _ptr(out["accepted_len"]), _ptr(out["out_tokens"]), _ptr(out["accept_prob"]),
+                                        _ptr(out["token_probs"]), _ptr(out["len_hist"]), _ptr(out["out_hidden"]),
+                                        _ptr(out["offsets"]), _ptr(out["next_tokens"]), _ptr(out["dev_error"]),
+                                        _ptr(ws), ws.numel(), _stream(stream))
+    if st != SPEC_OK:
+        raise SpecError("spec_verify_linear_compact", st)
     return out
 
 

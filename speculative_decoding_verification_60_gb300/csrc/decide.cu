@@ -1,88 +1,32 @@
 // Linear verification, stage 2 ("Accelerating Sonar through speculation",
 // §Speculative decoding and §Target-Draft; the cited rule): per request the
-// accept tests u_i < p(d_i) / q(d_i) in order, the accepted length, and the
 // draw from norm(max(0, p - q)) at the first rejection or from the last
-// target row after a full accept.  Built with 512-thread CTAs: one request
-// per CTA, so more warps per request shorten its draw.
+// target row after a full accept (the accept tests and the accepted length
+// come from the statistics launch), and the optional compaction.  Built
+// with 512-thread CTAs: one request per CTA, so more warps per request
+// shorten its draw.
 #include "launch.cuh"
 #include "linear_args.cuh"
 #include "sample.cuh"
 
 namespace sv {
 
-// One CTA per request: warp 0 takes the accept decisions, then the whole
-// CTA draws the residual or bonus token.
+// One CTA per request: the residual or bonus draw at the request's accept
+// decisions (taken by the statistics launch), its output tokens and, for
+// the compacting call, its accepted hidden rows and their next tokens at
+// the packed offset (§MTP: token t_{i+1} pairs with hidden state H_i;
+// §MTP schedule for a single token: the next tokens are inserted on the
+// GPU, without a host round trip).
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
     __shared__ BlockScratch s;
     __shared__ DrawScratch ds;
-    __shared__ int sh_a, sh_inval;
     const int b = blockIdx.x, k = a.k, V = a.V;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t req = a.req ? a.req[b] : (int64_t)b;
     const int64_t pos = a.pos ? a.pos[b] : 0;
     const int32_t* d = a.drafts + (size_t)b * k;
-
-    if (warp == 0) {
-        int inval = 0;
-        for (int i = lane; i <= k; i += 32)
-            if (a.stats[tgt_row(a, b, i)].flags & kRowInvalid) inval |= kDevErrNonfinite;
-        if (MODE > 0)
-            for (int i = lane; i < k; i += 32)
-                if (a.stats[drf_row(a, b, i)].flags & kRowInvalid) inval |= kDevErrNonfinite;
-        for (int i = lane; i < k; i += 32)
-            if (d[i] < 0 || d[i] >= V) inval |= kDevErrToken;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) inval |= __shfl_xor_sync(0xffffffffu, inval, o);
-        int first_reject = k;
-        for (int i0 = 0; i0 < k; i0 += 32) {
-            const int i = i0 + lane;
-            bool acc = true;
-            float ap = 0.0f, pp = 0.0f, qq = 0.0f;
-            if (i < k && !inval) {
-                const RowStat sp = a.stats[tgt_row(a, b, i)];
-                if (MODE == 0) {
-                    acc = (d[i] == sp.argmax);
-                    ap = acc ? 1.0f : 0.0f;
-                    pp = ap;
-                    qq = 1.0f;
-                } else {
-                    const RowStat sq = a.stats[drf_row(a, b, i)];
-                    const bool pm = (sp.flags & kRowTokMember) != 0, qm = (sq.flags & kRowTokMember) != 0;
-                    const float lp = fmaf(sp.x_tok, a.c, -scaled_max(sp.m, a.c));  // log2 of the weights
-                    const float lq = fmaf(sq.x_tok, a.c, -scaled_max(sq.m, a.c));
-                    pp = pm ? ex2(lp) * sp.inv_zn : 0.0f;
-                    qq = qm ? ex2(lq) * sq.inv_zn : 0.0f;
-                    // q = 0 (the token outside q's nucleus) rejects; a weight
-                    // that only underflowed in fp32 takes the ratio from the
-                    // logits, differenced before scaling (the exponents
-                    // themselves are large and would lose digits)
-                    float ratio = 0.0f;
-                    if (pm && qm)
-                        ratio = (pp > 0.0f && qq > 0.0f)
-                                    ? pp / qq
-                                    : ex2(((sp.x_tok - sq.x_tok) - (sp.m - sq.m)) * a.c) * (sp.inv_zn / sq.inv_zn);
-                    ap = fminf(1.0f, ratio);
-                    acc = uniform01(a.seed, req, pos + i + 1, kPurposeAccept, 0) < ratio;
-                }
-            }
-            if (i < k) {
-                if (a.accept_prob) a.accept_prob[(size_t)b * k + i] = inval ? 0.0f : ap;
-                if (a.token_probs) {
-                    a.token_probs[((size_t)b * k + i) * 2 + 0] = inval ? 0.0f : pp;
-                    a.token_probs[((size_t)b * k + i) * 2 + 1] = inval ? 0.0f : qq;
-                }
-            }
-            const unsigned rej = __ballot_sync(0xffffffffu, i < k && !acc);
-            if (rej && first_reject == k) first_reject = i0 + __ffs(rej) - 1;
-        }
-        if (lane == 0) {
-            sh_a = inval ? 0 : first_reject;
-            sh_inval = inval;
-        }
-    }
-    __syncthreads();
-    const int acnt = sh_a, inval = sh_inval;
+    const int dv = a.dec[b];
+    const int acnt = dv & 0xffff, inval = dv >> 16;
     const T* tgt = static_cast<const T*>(a.tgt) + (size_t)b * (k + 1) * V;
     int t = -1;
     if (inval) {
@@ -107,11 +51,27 @@ __global__ void __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
         }
     }
     if (threadIdx.x == 0) {
-        a.acc_len[b] = acnt;
         int32_t* o = a.out_tokens + (size_t)b * (k + 1);
         for (int j = 0; j <= k; ++j) o[j] = (j < acnt) ? d[j] : (j == acnt ? t : -1);
-        if (a.len_hist) atomicAdd(a.len_hist + acnt, 1);
-        if (inval && a.dev_error) atomicOr(a.dev_error, inval);
+    }
+    if (a.hidden) {  // rows 0 .. a of this request, packed at its offset
+        const int off = a.woff[b];
+        for (int r = 0; r <= acnt; ++r) {
+            const uint16_t* in = a.hidden + ((size_t)b * (k + 1) + r) * a.H;
+            uint16_t* out = a.out_hidden + (size_t)(off + r) * a.H;
+            if (a.vec_ok) {
+                const uint4* vi = reinterpret_cast<const uint4*>(in);
+                uint4* vo = reinterpret_cast<uint4*>(out);
+                for (int i = threadIdx.x; i < a.H / 8; i += kNT) vo[i] = __ldg(vi + i);
+            } else {
+                for (int i = threadIdx.x; i < a.H; i += kNT) out[i] = in[i];
+            }
+        }
+        if (threadIdx.x == 0) {
+            for (int r = 0; r <= acnt; ++r) a.next_tokens[off + r] = (r < acnt) ? d[r] : t;
+            a.offsets[b + 1] = a.woff[b + 1];
+            if (b == 0) a.offsets[0] = 0;
+        }
     }
 }
 

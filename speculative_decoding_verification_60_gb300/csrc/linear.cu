@@ -1,11 +1,13 @@
 // Linear verification ("Accelerating Sonar through speculation",
 // §Speculative decoding and §Target-Draft): row statistics of every target
-// and draft row (this file), then per request the accept tests, the
-// accepted length and the residual or bonus draw (decide.cu); the C entry
-// points.
+// and draft row, and in the last CTA of that launch every request's accept
+// tests, accepted length and packed offsets (this file); then per request
+// the residual or bonus draw and, for the compacting call, the gather of the
+// accepted positions' hidden rows (decide.cu); the C entry points.
 #include <mutex>
 
 #include "../../include/specverify.h"
+#include "decisions.cuh"
 #include "launch.cuh"
 #include "linear_args.cuh"
 #include "sample.cuh"
@@ -13,19 +15,31 @@
 namespace sv {
 
 // One CTA per row (persistent).  MODE 0 greedy, 1 sampled, 2 sampled + top-p.
-// redo_only: take only the rows the one-read top-p kernel marked kRowRedo.
+// finish = 0: every row.  finish = 1: the launch after the statistics
+// (every row written by an earlier launch): when some rows were left by the
+// one-read top-p pass it recomputes them and its last CTA then takes every
+// request's decisions; otherwise each warp takes one request's decisions at
+// once.  Either way the last CTA to finish writes the packed offsets.
 template <typename T, int MODE>
-__global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a, int redo_only) {
+__global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a, int finish) {
     extern __shared__ uint4 dyn_smem[];
     __shared__ BlockScratch s;
     __shared__ SampleScratch ss;
+    __shared__ unsigned sh_ticket;
     uint8_t* topsmem = reinterpret_cast<uint8_t*>(dyn_smem);
     const int nt = a.B * (a.k + 1);
     const int R = nt + (MODE > 0 ? a.B * a.k : 0);
     const T* tgt = static_cast<const T*>(a.tgt);
     const T* drf = static_cast<const T*>(a.drf);
+    const bool redo = finish && __ldcg(a.done + 2) != 0u;  // the same value in every thread
+    if (finish && !redo) {  // every record final: one warp per request
+        const int warp = threadIdx.x >> 5;
+        for (int b = blockIdx.x * kNW + warp; b < a.B; b += gridDim.x * kNW) warp_request_decisions<MODE>(a, b);
+        if (last_cta_done(a, &sh_ticket, 0)) linear_offsets(a, s);
+        return;
+    }
     for (int r = blockIdx.x; r < R; r += gridDim.x) {
-        if (redo_only && !(a.stats[r].flags & kRowRedo)) continue;  // the same value in every thread
+        if (redo && !(a.stats[r].flags & kRowRedo)) continue;  // the same value in every thread
         const T* row;
         int tok;
         if (r < nt) {
@@ -41,25 +55,35 @@ __global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a, int re
         if (threadIdx.x == 0) a.stats[r] = st;
         __syncthreads();
     }
+    if (finish && last_cta_done(a, &sh_ticket, 0)) {  // the recomputed rows are in: every request
+        const int warp = threadIdx.x >> 5;
+        for (int b = warp; b < a.B; b += kNW) warp_request_decisions<MODE>(a, b);
+        __syncthreads();
+        linear_offsets(a, s);
+    }
 }
 
-// Stage 1: statistics of every target and draft row into the workspace.
-// bf16 rows under top-p take the one-read kernel (rows_topp.cu) first; the
-// two-pass kernel then takes only the rows it left.
+// Stage 1: statistics of every target and draft row into the workspace,
+// then the finishing launch (decisions and offsets).  bf16 rows under top-p
+// take the one-read kernel (rows_topp.cu) first; the finishing launch then
+// also recomputes the rows it left.
 template <typename T, int MODE>
 static spec_status launch_stats(LinearArgs& a, cudaStream_t st) {
     const int nt = a.B * (a.k + 1);
     const int R = nt + (MODE > 0 ? a.B * a.k : 0);
     constexpr bool kOnePass = (MODE == 2 && sizeof(T) == 2);
-    if (kOnePass) {
-        const spec_status r = launch_rows_topp_onepass(a, st);
-        if (r != SPEC_OK) return r;
-    }
-    const size_t dyn = kOnePass ? (size_t)kTopSmemBytes : 0;
+    const size_t dyn = (MODE == 2 && sizeof(T) == 2) ? (size_t)kTopSmemBytes : 0;
     auto* k1 = k_linear_rowstats<T, MODE>;
     int grid = 0;
     if (!launch_grid(k1, dyn, R, &grid, kNT)) return SPEC_ERR_CUDA;
-    k1<<<grid, kNT, dyn, st>>>(a, kOnePass ? 1 : 0);
+    if (kOnePass) {
+        const spec_status r = launch_rows_topp_onepass(a, st);
+        if (r != SPEC_OK) return r;
+    } else {
+        k1<<<grid, kNT, dyn, st>>>(a, 0);
+        if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+    }
+    k1<<<grid, kNT, dyn, st>>>(a, 1);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -88,8 +112,8 @@ static spec_status prepare_linear(const void* target_logits, const void* draft_l
     if (!greedy && !draft_logits) return SPEC_ERR_INVALID_ARG;
     if ((int64_t)V > kMaxVocab) return SPEC_ERR_UNSUPPORTED;
     if ((int64_t)B * (2 * k + 1) > 0x7fffffffLL / 2) return SPEC_ERR_UNSUPPORTED;
-    const size_t need = spec_workspace_size(SPEC_OP_LINEAR, B, k, V, dtype);
-    if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+    const LinearWorkspace lw = linear_workspace(B, k);
+    if (!workspace || workspace_bytes < lw.total || (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return SPEC_ERR_WORKSPACE;
     if (!select_device_of(target_logits)) return SPEC_ERR_INVALID_ARG;
     a = LinearArgs{};
@@ -103,7 +127,11 @@ static spec_status prepare_linear(const void* target_logits, const void* draft_l
     a.top_p = top_p;
     a.c = greedy ? 0.0f : (float)(1.4426950408889634 / (double)T);
     a.seed = params->seed;
-    a.stats = static_cast<RowStat*>(workspace);
+    char* w = static_cast<char*>(workspace);
+    a.stats = reinterpret_cast<RowStat*>(w);
+    a.dec = reinterpret_cast<int32_t*>(w + lw.dec);
+    a.woff = reinterpret_cast<int32_t*>(w + lw.woff);
+    a.done = reinterpret_cast<unsigned*>(w + lw.done);
     mode = greedy ? 0 : (top_p < 1.0f ? 2 : 1);
     return SPEC_OK;
 }
@@ -116,15 +144,15 @@ static spec_status run_stage(LinearArgs& a, spec_dtype dtype, int mode, int stag
 
 using namespace sv;
 
-extern "C" spec_status spec_verify_linear(const void* target_logits, const void* draft_logits, spec_dtype dtype,
-                                          const int32_t* draft_tokens, int B, int k, int V,
-                                          const int64_t* request_ids, const int64_t* positions,
-                                          const spec_sampling_params* params, int32_t* accepted_len,
-                                          int32_t* out_tokens, float* accept_prob, float* token_probs,
-                                          int32_t* len_hist, int32_t* dev_error, void* workspace,
-                                          size_t workspace_bytes, spec_stream_t stream) {
+extern "C" spec_status spec_linear_stats_decide(const void* target_logits, const void* draft_logits,
+                                                spec_dtype dtype, const int32_t* draft_tokens, int B, int k, int V,
+                                                const int64_t* request_ids, const int64_t* positions,
+                                                const spec_sampling_params* params, int32_t* accepted_len,
+                                                float* accept_prob, float* token_probs, int32_t* len_hist,
+                                                int32_t* dev_error, void* workspace, size_t workspace_bytes,
+                                                spec_stream_t stream) {
     DeviceGuard device_guard;  // the caller's current device is put back on return
-    if (!accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
+    if (!accepted_len) return SPEC_ERR_INVALID_ARG;
     LinearArgs a;
     int mode = 0;
     spec_status r = prepare_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
@@ -134,55 +162,82 @@ extern "C" spec_status spec_verify_linear(const void* target_logits, const void*
     if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
     if (len_hist && cudaMemsetAsync(len_hist, 0, sizeof(int32_t) * (size_t)(k + 1), st) != cudaSuccess)
         return SPEC_ERR_CUDA;
+    if (cudaMemsetAsync(a.done, 0, 4 * sizeof(unsigned), st) != cudaSuccess) return SPEC_ERR_CUDA;
     a.acc_len = accepted_len;
-    a.out_tokens = out_tokens;
     a.accept_prob = accept_prob;
     a.token_probs = token_probs;
     a.len_hist = len_hist;
     a.dev_error = dev_error;
-    r = run_stage(a, dtype, mode, 0, st);
-    if (r != SPEC_OK) return r;
-    return run_stage(a, dtype, mode, 1, st);
+    return run_stage(a, dtype, mode, 0, st);
 }
 
-extern "C" spec_status spec_linear_stats(const void* target_logits, const void* draft_logits, spec_dtype dtype,
-                                         const int32_t* draft_tokens, int B, int k, int V,
-                                         const spec_sampling_params* params, void* workspace, size_t workspace_bytes,
-                                         spec_stream_t stream) {
+extern "C" spec_status spec_linear_draw(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                        const int32_t* draft_tokens, int B, int k, int V,
+                                        const int64_t* request_ids, const int64_t* positions,
+                                        const spec_sampling_params* params, const void* hidden, int H,
+                                        int32_t* out_tokens, void* out_hidden, int32_t* offsets,
+                                        int32_t* next_tokens, const void* workspace, size_t workspace_bytes,
+                                        spec_stream_t stream) {
     DeviceGuard device_guard;  // the caller's current device is put back on return
-    LinearArgs a;
-    int mode = 0;
-    const spec_status r = prepare_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, nullptr, nullptr,
-                                         params, workspace, workspace_bytes, a, mode);
-    if (r != SPEC_OK) return r;
-    return run_stage(a, dtype, mode, 0, reinterpret_cast<cudaStream_t>(stream));
-}
-
-extern "C" spec_status spec_linear_decide(const void* target_logits, const void* draft_logits, spec_dtype dtype,
-                                          const int32_t* draft_tokens, int B, int k, int V,
-                                          const int64_t* request_ids, const int64_t* positions,
-                                          const spec_sampling_params* params, int32_t* accepted_len,
-                                          int32_t* out_tokens, float* accept_prob, float* token_probs,
-                                          int32_t* len_hist, int32_t* dev_error, const void* workspace,
-                                          size_t workspace_bytes, spec_stream_t stream) {
-    DeviceGuard device_guard;  // the caller's current device is put back on return
-    if (!accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
+    if (!out_tokens) return SPEC_ERR_INVALID_ARG;
+    if (hidden && (H < 1 || !out_hidden || !offsets || !next_tokens)) return SPEC_ERR_INVALID_ARG;
+    if (hidden && (int64_t)B * (k + 1) >= 0x7fffffffLL) return SPEC_ERR_UNSUPPORTED;
     LinearArgs a;
     int mode = 0;
     spec_status r = prepare_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
                                    params, const_cast<void*>(workspace), workspace_bytes, a, mode);
     if (r != SPEC_OK) return r;
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (len_hist && cudaMemsetAsync(len_hist, 0, sizeof(int32_t) * (size_t)(k + 1), st) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-    a.acc_len = accepted_len;
     a.out_tokens = out_tokens;
-    a.accept_prob = accept_prob;
-    a.token_probs = token_probs;
-    a.len_hist = len_hist;
-    a.dev_error = dev_error;
-    return run_stage(a, dtype, mode, 1, st);
+    if (hidden) {
+        a.hidden = static_cast<const uint16_t*>(hidden);
+        a.H = H;
+        a.out_hidden = static_cast<uint16_t*>(out_hidden);
+        a.offsets = offsets;
+        a.next_tokens = next_tokens;
+        a.vec_ok = ((size_t)H * 2) % 16 == 0 && (reinterpret_cast<uintptr_t>(hidden) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(out_hidden) & 15u) == 0;
+    }
+    return run_stage(a, dtype, mode, 1, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" spec_status spec_verify_linear(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                          const int32_t* draft_tokens, int B, int k, int V,
+                                          const int64_t* request_ids, const int64_t* positions,
+                                          const spec_sampling_params* params, int32_t* accepted_len,
+                                          int32_t* out_tokens, float* accept_prob, float* token_probs,
+                                          int32_t* len_hist, int32_t* dev_error, void* workspace,
+                                          size_t workspace_bytes, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
+    if (!accepted_len || !out_tokens) return SPEC_ERR_INVALID_ARG;
+    const spec_status r =
+        spec_linear_stats_decide(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
+                                 params, accepted_len, accept_prob, token_probs, len_hist, dev_error, workspace,
+                                 workspace_bytes, stream);
+    if (r != SPEC_OK) return r;
+    return spec_linear_draw(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
+                            params, nullptr, 0, out_tokens, nullptr, nullptr, nullptr, workspace, workspace_bytes,
+                            stream);
+}
+
+extern "C" spec_status spec_verify_linear_compact(const void* target_logits, const void* draft_logits,
+                                                  spec_dtype dtype, const int32_t* draft_tokens, int B, int k, int V,
+                                                  const int64_t* request_ids, const int64_t* positions,
+                                                  const spec_sampling_params* params, const void* hidden, int H,
+                                                  int32_t* accepted_len, int32_t* out_tokens, float* accept_prob,
+                                                  float* token_probs, int32_t* len_hist, void* out_hidden,
+                                                  int32_t* offsets, int32_t* next_tokens, int32_t* dev_error,
+                                                  void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
+    if (!accepted_len || !out_tokens || !hidden || H < 1 || !out_hidden || !offsets || !next_tokens)
+        return SPEC_ERR_INVALID_ARG;
+    const spec_status r =
+        spec_linear_stats_decide(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
+                                 params, accepted_len, accept_prob, token_probs, len_hist, dev_error, workspace,
+                                 workspace_bytes, stream);
+    if (r != SPEC_OK) return r;
+    return spec_linear_draw(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
+                            params, hidden, H, out_tokens, out_hidden, offsets, next_tokens, workspace,
+                            workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -194,17 +249,22 @@ extern "C" spec_status spec_linear_decide(const void* target_logits, const void*
 // fixed array that lives in the library's device image, so the caller only
 // passes inputs and outputs.
 //
-// The array holds kNoAllocMaxRows rows (2 MiB); every GPU that loads the
-// library keeps it until the process exits.  Calls with B * (2k + 1) rows
-// above that limit return SPEC_ERR_UNSUPPORTED.  All calls share the array,
-// so calls that overlap on the GPU (on different streams, or from different
-// host threads) race on it.  Each call writes every row's statistics before
-// reading them, so nothing in the array needs to start at zero.
+// The array holds the workspace of up to kNoAllocMaxRows rows (about 2.3
+// MiB: the row records, the decisions, the offsets and a counter); every GPU
+// that loads the library keeps it until the process exits.  Calls with
+// B * (2k + 1) rows above that limit return SPEC_ERR_UNSUPPORTED.  All calls
+// share the array, so calls that overlap on the GPU (on different streams,
+// or from different host threads) race on it.  Each call clears the counter
+// and writes every record before reading it, so nothing in the array needs
+// to start at zero.
 // ---------------------------------------------------------------------------
 namespace sv {
 
 constexpr int kNoAllocMaxRows = 65536;
-static __device__ __align__(256) RowStat g_noalloc_stats[kNoAllocMaxRows];
+// every (B, k) within the row limit has B <= kNoAllocMaxRows / 3
+constexpr size_t kNoAllocMaxB = kNoAllocMaxRows / 3;
+constexpr size_t kNoAllocBytes = kNoAllocMaxRows * sizeof(RowStat) + 2 * (((kNoAllocMaxB + 1) * 4 + 255) / 256 * 256) + 256;
+static __device__ __align__(256) uint8_t g_noalloc_stats[kNoAllocBytes];
 
 constexpr int kNoAllocMaxDevices = 64;
 static std::mutex g_noalloc_mutex;
@@ -237,11 +297,12 @@ extern "C" spec_status spec_verify_linear_noalloc(const void* target_logits, con
     DeviceGuard device_guard;  // the caller's current device is put back on return
     if (B < 1 || k < 1 || V < 1) return SPEC_ERR_INVALID_ARG;
     if ((int64_t)B * (2 * (int64_t)k + 1) > kNoAllocMaxRows) return SPEC_ERR_UNSUPPORTED;
+    if (linear_workspace(B, k).total > kNoAllocBytes) return SPEC_ERR_UNSUPPORTED;
     if (!target_logits || !select_device_of(target_logits)) return SPEC_ERR_INVALID_ARG;
     void* scratch = nullptr;
     const spec_status r = noalloc_scratch(&scratch);
     if (r != SPEC_OK) return r;
     return spec_verify_linear(target_logits, draft_logits, dtype, draft_tokens, B, k, V, request_ids, positions,
                               params, accepted_len, out_tokens, accept_prob, token_probs, len_hist, dev_error,
-                              scratch, sizeof(RowStat) * (size_t)kNoAllocMaxRows, stream);
+                              scratch, kNoAllocBytes, stream);
 }

@@ -335,11 +335,15 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
             }
         }
         if (redo) st.flags = kRowRedo;
-        if (tid == 0) a.stats[r] = st;
+        if (tid == 0) {
+            a.stats[r] = st;
+            if (redo && a.dec) atomicAdd(a.done + 2, 1u);
+        }
         if (abort_row) {  // leave every remaining row to the two-pass kernel
             if (tid == 0) {
                 if (a.dev_error) atomicOr(a.dev_error, kDevErrTimeout);
                 for (int r2 = r + gridDim.x; r2 < R; r2 += gridDim.x) a.stats[r2].flags = kRowRedo;
+                if (a.dec) atomicAdd(a.done + 2, 1u);
             }
             break;
         }

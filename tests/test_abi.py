@@ -80,6 +80,16 @@ def test_host_argument_checks_return_status(lib):
     assert lib.spec_verify_tree(dummy, dummy, 0, dummy, dummy, 1, 3, 8, 3, None, None, ctypes.byref(sp),
                                 dummy, dummy, dummy, None, dummy, 256, None) == 1
     assert lib.spec_compact_accepted(None, 1, 1, 8, dummy, None, dummy, 1, dummy, dummy, dummy, None, None) == 1
+    # the compacting call needs its hidden buffers; the split calls check like the one-call form
+    assert lib.spec_verify_linear_compact(dummy, dummy, 0, dummy, 1, 1, 8, None, None, ctypes.byref(sp), None, 16,
+                                          dummy, dummy, None, None, None, dummy, dummy, dummy, None, dummy, 1 << 20,
+                                          None) == 1
+    assert lib.spec_linear_stats_decide(dummy, dummy, 0, dummy, 1, 1, 8, None, None, ctypes.byref(sp), None,
+                                        None, None, None, None, dummy, 1 << 20, None) == 1
+    assert lib.spec_linear_draw(dummy, dummy, 0, dummy, 1, 1, 8, None, None, ctypes.byref(sp), None, 0, None,
+                                None, None, None, dummy, 1 << 20, None) == 1
+    assert lib.spec_linear_stats_decide(dummy, dummy, 0, dummy, 1, 65, 8, None, None, ctypes.byref(sp), dummy,
+                                        None, None, None, None, dummy, 1 << 20, None) == 2
 
 
 def test_sample_rows_host_checks(lib):
