@@ -38,7 +38,7 @@ TREE_WORKLOAD = "tree-b32-n60-k4-d5-v128256"
 HIDDEN = 7168
 METRIC = "verified logit rows/s at V=128256 bf16; achieved HBM GB/s vs GB300 peak"
 UNIT = "rows/s"
-PROFILE = os.path.join(ROOT, "profiles", "k_linear_rowstats_linear-b256-k8-v128256-t0.7-p0.9.txt")
+PROFILE = os.path.join(ROOT, "profiles", "k_rows_topp_onepass_linear-b256-k8-v128256-t0.7-p0.9.txt")
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -93,11 +93,11 @@ def job_value(rows_per_rank: int, world: int, ms: float) -> float:
 
 
 def source_sha() -> str:
-    """Hash of the row-statistics kernel's sources (linear.cu and every
-    kernel header it includes, transitively), to tell whether recorded
-    counters still apply."""
+    """Hash of the dominant kernel's sources (rows_topp.cu, the one-read
+    top-p row statistics, and every kernel header it includes,
+    transitively), to tell whether recorded counters still apply."""
     csrc = os.path.join(ROOT, "speculative_decoding_verification_60_gb300", "csrc")
-    seen, todo = set(), ["linear.cu"]
+    seen, todo = set(), ["rows_topp.cu"]
     while todo:
         f = todo.pop()
         if f in seen or not os.path.exists(os.path.join(csrc, f)):
@@ -115,9 +115,9 @@ def source_sha() -> str:
 
 
 def recorded_traffic():
-    """DRAM bytes per launch of the row-statistics kernel from the committed
-    ncu summary, or None when that summary is missing or was taken on other
-    kernel sources."""
+    """DRAM bytes per launch of the one-read row-statistics kernel from the
+    committed ncu summary, or None when that summary is missing or was taken
+    on other kernel sources."""
     if not os.path.exists(PROFILE):
         return None
     kv = {}
@@ -625,14 +625,17 @@ def run_ours(args):
                    "top_p": step.top_p, "hidden": HIDDEN, "rows_per_step": step.B * (2 * step.k + 1),
                    "l2": "inputs larger than L2 (1116 MB of logits per step, L2 129 MB)",
                    "parallelism": f"dp{world} (independent request shards)" if world > 1 else "1 GPU"},
-        "roofline": {"bound": "hbm", "kernel": "k_linear_rowstats", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": "k_rows_topp_onepass",
+                     "timed": "the row-statistics call: the one-read pass and the finishing launch (decisions, "
+                              "offsets), events on its stream", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_kind": peak_kind, "traffic": recorded_traffic(),
                      "algorithmic_bytes_per_launch": step.algo_bytes, "launch_ms": round(stats_ms, 4)},
-        "e2e": {"value": round(job_value(rows, world, e2e_ms), 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "pipeline": f"{chunks} request groups, copy of group i+1 overlapping verification of group i",
-                "dev_error": e2e_err},
+        "e2e": None if args.no_e2e else {
+            "value": round(job_value(rows, world, e2e_ms), 1), "unit": UNIT, "ms_per_step": round(e2e_ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "pipeline": f"{chunks} request groups, copy of group i+1 overlapping verification of group i",
+            "dev_error": e2e_err},
         "gpu_launches": launches,
         "clocks": clk,
         "mean_accepted_len": round(float(acc.float().mean()), 4),

@@ -1,7 +1,7 @@
 """bench.py's link between the committed ncu summary and the current kernel
-sources: the recorded DRAM traffic is reported only while the row-statistics
-kernel's sources (linear.cu and the kernel headers it includes) are those the
-capture was taken on."""
+sources: the recorded DRAM traffic is reported only while the one-read
+row-statistics kernel's sources (rows_topp.cu and the kernel headers it
+includes) are those the capture was taken on."""
 
 import os
 import shutil
@@ -24,6 +24,7 @@ def test_hash_follows_the_row_statistics_sources_only(tmp_path, monkeypatch):
     h0 = bench.source_sha()
     # a unit the kernel does not include leaves the hash alone
     (csrc / "compact.cu").write_text((csrc / "compact.cu").read_text() + "\n// edit\n")
+    (csrc / "linear.cu").write_text((csrc / "linear.cu").read_text() + "\n// edit\n")
     (csrc / "unrelated.cu").write_text("// another unit\n")
     assert bench.source_sha() == h0
     # a header the kernel includes (transitively) changes it
