@@ -7,6 +7,7 @@
 // shorten its draw.
 #include "launch.cuh"
 #include "linear_args.cuh"
+#include "draw_bf16.cuh"
 #include "sample.cuh"
 
 namespace sv {
@@ -20,7 +21,10 @@ namespace sv {
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
     __shared__ BlockScratch s;
-    __shared__ DrawScratch ds;
+    __shared__ union {
+        DrawScratch d;    // fp32 rows
+        BDrawScratch b;   // bf16 rows
+    } ds;
     const int b = blockIdx.x, k = a.k, V = a.V;
     const int64_t req = a.req ? a.req[b] : (int64_t)b;
     const int64_t pos = a.pos ? a.pos[b] : 0;
@@ -37,17 +41,28 @@ __global__ void __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
         const RowStat sp = a.stats[tgt_row(a, b, acnt)];
         const T* prow = tgt + (size_t)acnt * V;
         const RowView<T> rv(prow, V);
-        FilteredRow<T> P(prow, sp, a.c, 0x7fffffff);
         const bool resid = acnt < k;
         const float u = uniform01(a.seed, req, pos + acnt + 1, resid ? kPurposeResidual : kPurposeBonus, 0);
-        if (resid) {
-            const RowStat sq = a.stats[drf_row(a, b, acnt)];
-            const T* qrow = static_cast<const T*>(a.drf) + ((size_t)b * k + acnt) * V;
-            FilteredRow<T> Q(qrow, sq, a.c, 0x7fffffff);
-            t = draw_linear<T, true, (MODE == 2)>(rv, P, Q, u, s, ds);
-            if (t < 0) t = draw_linear<T, false, (MODE == 2)>(rv, P, Q, u, s, ds);  // p == q: draw from p
+        const RowStat sq = resid ? a.stats[drf_row(a, b, acnt)] : sp;
+        const T* qrow = resid ? static_cast<const T*>(a.drf) + ((size_t)b * k + acnt) * V : prow;
+        if constexpr (sizeof(T) == 2) {
+            BRow P(reinterpret_cast<const uint16_t*>(prow), sp, a.c, MODE == 2);
+            if (resid) {
+                BRow Q(reinterpret_cast<const uint16_t*>(qrow), sq, a.c, MODE == 2);
+                t = draw_linear_bf16<true, (MODE == 2)>(rv, P, Q, a.c, u, s, ds.b);
+                if (t < 0) t = draw_linear_bf16<false, (MODE == 2)>(rv, P, P, a.c, u, s, ds.b);  // p == q: draw from p
+            } else {
+                t = draw_linear_bf16<false, (MODE == 2)>(rv, P, P, a.c, u, s, ds.b);
+            }
         } else {
-            t = draw_linear<T, false, (MODE == 2)>(rv, P, P, u, s, ds);
+            FilteredRow<T> P(prow, sp, a.c, 0x7fffffff);
+            if (resid) {
+                FilteredRow<T> Q(qrow, sq, a.c, 0x7fffffff);
+                t = draw_linear<T, true, (MODE == 2)>(rv, P, Q, u, s, ds.d);
+                if (t < 0) t = draw_linear<T, false, (MODE == 2)>(rv, P, Q, u, s, ds.d);  // p == q: draw from p
+            } else {
+                t = draw_linear<T, false, (MODE == 2)>(rv, P, P, u, s, ds.d);
+            }
         }
     }
     if (threadIdx.x == 0) {
