@@ -12,12 +12,12 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["api.cu", "linear.cu", "rows_topp.cu", "decide.cu", "tree.cu", "compact.cu", "sample_rows.cu"]
+SOURCES = ["api.cu", "linear.cu", "rows_topp.cu", "decide.cu", "draw_stream.cu", "tree.cu", "compact.cu", "sample_rows.cu"]
 # threads per CTA of the row-level kernels in each unit (see common.cuh)
 CTA_THREADS = {"decide.cu": 512, "tree.cu": 512, "sample_rows.cu": 512}
 # units whose CTAs hold a copy warp beside the row threads: row barriers are
 # named barriers over the row threads only
-NAMED_ROW_BARRIER = {"rows_topp.cu"}
+NAMED_ROW_BARRIER = {"rows_topp.cu", "draw_stream.cu"}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -104,6 +104,7 @@ static spec_status launch_decide_t(LinearArgs& a, int mode, cudaStream_t st) {
 }
 
 spec_status launch_decide_stage(LinearArgs& a, spec_dtype dtype, int mode, cudaStream_t st) {
+    if (dtype == SPEC_BF16 && draw_stream_applies(a, mode)) return launch_draw_stream(a, mode, st);
     return dtype == SPEC_BF16 ? launch_decide_t<__nv_bfloat16>(a, mode, st) : launch_decide_t<float>(a, mode, st);
 }
 

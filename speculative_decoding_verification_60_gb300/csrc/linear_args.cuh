@@ -65,6 +65,11 @@ __host__ __device__ inline LinearWorkspace linear_workspace(int B, int k) {
 // it cannot finish are marked kRowRedo for the two-pass kernel.
 spec_status launch_rows_topp_onepass(LinearArgs& a, cudaStream_t st);
 
+// Stage 2 for bf16 sampled rows with 16-byte aligned units (draw_stream.cu):
+// the rows streamed through shared memory by bulk copies.
+bool draw_stream_applies(const LinearArgs& a, int mode);
+spec_status launch_draw_stream(LinearArgs& a, int mode, cudaStream_t st);
+
 // Stage 2 (decide.cu): the residual or bonus draw and the optional
 // compaction, one CTA per request.
 spec_status launch_decide_stage(LinearArgs& a, spec_dtype dtype, int mode, cudaStream_t st);
