@@ -40,7 +40,12 @@ struct LinearArgs {
     int32_t* offsets;        // [B+1]
     int32_t* next_tokens;    // [B*(k+1)]
     bool vec_ok;             // H*2 % 16 == 0 and both hidden pointers 16-byte aligned
+    // draft-side sampler on the one-read pass (B rows of logits in tgt, k = 0):
+    // the token of each row, or kSampleRedo for the two-pass sampler
+    int32_t* sample_out;
 };
+
+constexpr int32_t kSampleRedo = -2;
 
 __device__ __forceinline__ int tgt_row(const LinearArgs& a, int b, int i) { return b * (a.k + 1) + i; }
 __device__ __forceinline__ int drf_row(const LinearArgs& a, int b, int i) { return a.B * (a.k + 1) + b * a.k + i; }
@@ -64,6 +69,9 @@ __host__ __device__ inline LinearWorkspace linear_workspace(int B, int k) {
 // Stage 1 for bf16 rows under top-p (rows_topp.cu): one read per row; rows
 // it cannot finish are marked kRowRedo for the two-pass kernel.
 spec_status launch_rows_topp_onepass(LinearArgs& a, cudaStream_t st);
+// The draft-side sampler's first launch (rows_topp.cu): tokens of bf16 rows
+// under top-p in one read each; kSampleRedo where the row needs the two-pass route.
+spec_status launch_sample_onepass(LinearArgs& a, cudaStream_t st);
 
 // Stage 2 for bf16 sampled rows with 16-byte aligned units (draw_stream.cu):
 // the rows streamed through shared memory by bulk copies.

@@ -26,8 +26,15 @@
 // A row this route cannot finish exactly (m^ not above zero, a maximum
 // above the window, a boundary below it, a sum that is not finite, a wait
 // that ran out) is marked kRowRedo and the two-pass kernel recomputes it.
+//
+// The same pass serves the draft-side sampler (SAMPLE): the rows are plain
+// logit rows, and once a row's nucleus is known its token is drawn right
+// away from the row (just streamed, so read from L2) while the copy warp
+// already streams the next row; a row this route cannot finish gets the
+// mark kSampleRedo in place of its token for the two-pass sampler.
 #include "../../include/specverify.h"
 #include "bulk.cuh"
+#include "draw_bf16.cuh"
 #include "launch.cuh"
 #include "linear_args.cuh"
 #include "rowstats.cuh"
@@ -114,6 +121,9 @@ __device__ __forceinline__ void count_key(uint32_t xb, int lo, int hi, uint32_t 
     asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(hbk + (cb >> kCopyShift)) : "memory");
 }
 
+static_assert(sizeof(BDrawScratch) <= sizeof(uint32_t) * kWinKeys * kCopies, "the draw's scratch fits in the histogram");
+
+template <bool SAMPLE>
 __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_topp_onepass(LinearArgs a) {
     extern __shared__ __align__(128) uint8_t onepass_raw[];
     OnePassSmem& sm = *reinterpret_cast<OnePassSmem*>(onepass_raw);
@@ -335,14 +345,34 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
             }
         }
         if (redo) st.flags = kRowRedo;
-        if (tid == 0) {
-            a.stats[r] = st;
-            if (redo && a.dec) atomicAdd(a.done + 2, 1u);
+        if constexpr (SAMPLE) {
+            // the token at the DRAFT-purpose uniform, drawn from the row (in
+            // L2 now); the histogram's space holds the draw's scratch
+            int t = kSampleRedo;
+            if (!redo) {
+                const int64_t req = a.req ? a.req[r] : (int64_t)r;
+                const int64_t pos = a.pos ? a.pos[r] : 0;
+                const float u = uniform01(a.seed, req, pos, kPurposeDraft, 0);
+                BRow P(reinterpret_cast<const uint16_t*>(row), st, c, true);
+                t = draw_linear_bf16<false, true>(rv, P, P, c, u, sm.s, *reinterpret_cast<BDrawScratch*>(sm.hist));
+                if (t < 0) t = kSampleRedo;
+            }
+            if (tid == 0) a.sample_out[r] = t;
+        } else {
+            if (tid == 0) {
+                a.stats[r] = st;
+                if (redo && a.dec) atomicAdd(a.done + 2, 1u);
+            }
         }
         if (abort_row) {  // leave every remaining row to the two-pass kernel
             if (tid == 0) {
                 if (a.dev_error) atomicOr(a.dev_error, kDevErrTimeout);
-                for (int r2 = r + gridDim.x; r2 < R; r2 += gridDim.x) a.stats[r2].flags = kRowRedo;
+                for (int r2 = r + gridDim.x; r2 < R; r2 += gridDim.x) {
+                    if constexpr (SAMPLE)
+                        a.sample_out[r2] = kSampleRedo;
+                    else
+                        a.stats[r2].flags = kRowRedo;
+                }
                 if (a.dec) atomicAdd(a.done + 2, 1u);
             }
             break;
@@ -356,8 +386,16 @@ spec_status launch_rows_topp_onepass(LinearArgs& a, cudaStream_t st) {
     const long long R = (long long)a.B * (2 * a.k + 1);
     const size_t smem = sizeof(OnePassSmem);
     int grid = 0;
-    if (!launch_grid(k_rows_topp_onepass, smem, R, &grid, kOnePassThreads)) return SPEC_ERR_CUDA;
-    k_rows_topp_onepass<<<grid, kOnePassThreads, smem, st>>>(a);
+    if (!launch_grid(k_rows_topp_onepass<false>, smem, R, &grid, kOnePassThreads)) return SPEC_ERR_CUDA;
+    k_rows_topp_onepass<false><<<grid, kOnePassThreads, smem, st>>>(a);
+    return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}
+
+spec_status launch_sample_onepass(LinearArgs& a, cudaStream_t st) {
+    const size_t smem = sizeof(OnePassSmem);
+    int grid = 0;
+    if (!launch_grid(k_rows_topp_onepass<true>, smem, a.B, &grid, kOnePassThreads)) return SPEC_ERR_CUDA;
+    k_rows_topp_onepass<true><<<grid, kOnePassThreads, smem, st>>>(a);
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

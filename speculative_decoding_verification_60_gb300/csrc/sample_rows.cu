@@ -4,9 +4,12 @@
 // no host round trip).  One token per logit row from filter(softmax(row /
 // T)), by the same row statistics and inverse-CDF draw as the bonus token
 // of linear verification, with the DRAFT purpose in the Philox counter.
+// bf16 rows under top-p take the one-read pass first (rows_topp.cu), which
+// marks the rows it cannot finish; this kernel then takes only those.
 // Built with 512-thread CTAs: one row per CTA at a time.
 #include "../../include/specverify.h"
 #include "launch.cuh"
+#include "linear_args.cuh"
 #include "sample.cuh"
 
 namespace sv {
@@ -20,6 +23,7 @@ struct SampleArgs {
     uint64_t seed;
     int32_t* out;
     int32_t* dev_error;
+    bool redo_only;  // take only the rows whose out holds kSampleRedo
 };
 
 template <typename T, int MODE>
@@ -30,6 +34,7 @@ __global__ void __launch_bounds__(kNT, 2) k_sample_rows(SampleArgs a) {
     __shared__ DrawScratch ds;
     uint8_t* topsmem = reinterpret_cast<uint8_t*>(dyn_smem);
     for (int r = blockIdx.x; r < a.R; r += gridDim.x) {
+        if (a.redo_only && a.out[r] != kSampleRedo) continue;  // the same for the whole CTA
         const T* row = static_cast<const T*>(a.logits) + (size_t)r * a.V;
         const RowStat st = row_stats<T, MODE>(row, a.V, a.c, a.top_p, -1, topsmem, s, ss);
         int t;
@@ -103,5 +108,23 @@ extern "C" spec_status spec_sample_rows(const void* logits, spec_dtype dtype, in
     const int mode = greedy ? 0 : (top_p < 1.0f ? 2 : 1);
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (dtype == SPEC_BF16 && mode == 2) {
+        // one read per row, then the two-pass route on the rows it leaves
+        LinearArgs la{};
+        la.tgt = logits;
+        la.B = R;
+        la.k = 0;
+        la.V = V;
+        la.req = request_ids;
+        la.pos = positions;
+        la.c = a.c;
+        la.top_p = top_p;
+        la.seed = a.seed;
+        la.dev_error = dev_error;
+        la.sample_out = out_tokens;
+        const spec_status s1 = launch_sample_onepass(la, st);
+        if (s1 != SPEC_OK) return s1;
+        a.redo_only = true;
+    }
     return dtype == SPEC_BF16 ? launch_sample_t<__nv_bfloat16>(a, mode, st) : launch_sample_t<float>(a, mode, st);
 }
