@@ -262,10 +262,11 @@ class LinearStep:
         # one read of every target and draft row (greedy: target rows only)
         self.algo_bytes = B * ((2 * k + 1) if self.T > 0 else (k + 1)) * V * 2
         self.mode = 0 if self.T == 0 else (2 if self.top_p < 1.0 else 1)
-        # launches of one step: row statistics (one-read top-p pass, then the
-        # two-pass kernel on the rows it leaves, whose last CTA takes the
-        # decisions), then the draw with the compaction
-        self.launches_per_step = (2 if self.mode == 2 else 1) + 1
+        # launches of one step: the counters zeroed; the row statistics (the
+        # one-read top-p pass, or the two-pass kernel); the finishing launch
+        # (rows the one-read pass left, the decisions, the offsets); the draw
+        # with the compaction
+        self.launches_per_step = 4
 
     @staticmethod
     def P(t):
@@ -302,18 +303,26 @@ def time_linear(step: LinearStep, K: int, W: int, barrier):
     torch.cuda.synchronize()
     barrier()
     torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(s)
     for i in range(K):
-        ev[i][0].record(s)
         step.stats(s)
-        ev[i][1].record(s)
         step.draw_compact(s)
     e1.record(s)
     torch.cuda.synchronize()
     barrier()
     ms = e0.elapsed_time(e1) / K
+    # the row-statistics call timed on its own, in steps of the same kind
+    # (outside the timed steps: an event between two launches keeps the
+    # second from starting while the first ends)
+    K2 = min(K, 100)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K2)]
+    for i in range(K2):
+        ev[i][0].record(s)
+        step.stats(s)
+        ev[i][1].record(s)
+        step.draw_compact(s)
+    torch.cuda.synchronize()
     stats_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     return ms, stats_ms, step.launches_per_step * K
 
@@ -413,7 +422,7 @@ def time_sampler(step: LinearStep, K: int, W: int, peak: float):
     gbps = B * V * 2 / (ms / 1e3) / 1e9
     return {"workload": f"{B} rows of V={V} bf16, T={step.T}, top-p {step.top_p}", "ms": round(ms, 4),
             "rows_per_s": round(B / (ms / 1e3), 1), "gbps": round(gbps, 1), "frac": round(gbps / peak, 4),
-            "launches": K, "l2": "flushed before every launch"}
+            "launches": K * (2 if step.mode == 2 else 1), "l2": "flushed before every launch"}
 
 
 def time_tree(device, K: int, W: int, peak: float):

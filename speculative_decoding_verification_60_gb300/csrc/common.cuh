@@ -119,6 +119,13 @@ __device__ __forceinline__ uint32_t bf16_bits_round_down(float f) {
 // other warps beside them (a warp issuing bulk copies) defines
 // SV_ROW_BARRIER_NAMED, so that these barriers count the kNT row threads
 // only (named barrier 1); elsewhere they are the CTA barrier.
+// Programmatic dependent launch: a kernel lets the next kernel on its
+// stream be scheduled (grid_dep_trigger, called by every CTA), and a kernel
+// so launched waits for the one before it to complete and its writes to be
+// visible (grid_dep_wait; a no-op after an ordinary launch).
+__device__ __forceinline__ void grid_dep_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void row_sync() {
 #ifdef SV_ROW_BARRIER_NAMED
     asm volatile("bar.sync 1, %0;" ::"n"(kNT) : "memory");

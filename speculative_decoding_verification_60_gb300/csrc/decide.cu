@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
         BDrawScratch b;   // bf16 rows
     } ds;
     const int b = blockIdx.x, k = a.k, V = a.V;
+    grid_dep_wait();  // the decisions and offsets come from the launch before
     const int64_t req = a.req ? a.req[b] : (int64_t)b;
     const int64_t pos = a.pos ? a.pos[b] : 0;
     const int32_t* d = a.drafts + (size_t)b * k;
@@ -92,7 +93,7 @@ __global__ void __launch_bounds__(kNT, 2) k_linear_finalize(LinearArgs a) {
 
 template <typename T, int MODE>
 static spec_status launch_decide(LinearArgs& a, cudaStream_t st) {
-    k_linear_finalize<T, MODE><<<a.B, kNT, 0, st>>>(a);
+    if (launch_dependent(k_linear_finalize<T, MODE>, dim3(a.B), dim3(kNT), 0, st, a) != cudaSuccess) return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -141,6 +141,7 @@ __global__ void __launch_bounds__(kDThreads, 2) k_draw_stream(LinearArgs a) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x, k = a.k, V = a.V;
     const int nvec = V / 8;
+    grid_dep_wait();  // the decisions and offsets come from the launch before
     const int dv = a.dec[b];
     const int acnt = dv & 0xffff, inval = dv >> 16;
     const bool resid = acnt < k;
@@ -459,7 +460,7 @@ template <int MODE>
 spec_status launch_mode(LinearArgs& a, cudaStream_t st) {
     const size_t smem = sizeof(DrawSmem);
     if (!set_dyn_smem(k_draw_stream<MODE>, smem, kDThreads)) return SPEC_ERR_CUDA;
-    k_draw_stream<MODE><<<a.B, kDThreads, smem, st>>>(a);
+    if (launch_dependent(k_draw_stream<MODE>, dim3(a.B), dim3(kDThreads), smem, st, a) != cudaSuccess) return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -111,4 +111,25 @@ inline bool set_dyn_smem(K kernel, size_t dyn_smem, int block) {
     return launch_shape(reinterpret_cast<const void*>(kernel), dyn_smem, block, &sh);
 }
 
+// Launch that may overlap its start with the end of the kernel before it on
+// the stream (programmatic dependent launch): its CTAs are scheduled once
+// every CTA of that kernel has started (each calls grid_dep_trigger first),
+// and wait in grid_dep_wait, before reading anything it wrote, until it has
+// completed.  After any other stream operation it is an ordinary launch.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t dyn_smem, cudaStream_t st,
+                                    Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = dyn_smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 }  // namespace sv

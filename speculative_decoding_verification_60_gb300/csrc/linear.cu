@@ -31,6 +31,8 @@ __global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a, int fi
     const int R = nt + (MODE > 0 ? a.B * a.k : 0);
     const T* tgt = static_cast<const T*>(a.tgt);
     const T* drf = static_cast<const T*>(a.drf);
+    grid_dep_wait();     // the finishing launch reads what the launch before it wrote
+    grid_dep_trigger();  // the next launch may be scheduled; it waits for this grid
     const bool redo = finish && __ldcg(a.done + 2) != 0u;  // the same value in every thread
     if (finish && !redo) {  // every record final: one warp per request
         const int warp = threadIdx.x >> 5;
@@ -63,6 +65,18 @@ __global__ void __launch_bounds__(kNT, 4) k_linear_rowstats(LinearArgs a, int fi
     }
 }
 
+// Zeroes the call's counters, device error word and length histogram in
+// one launch (the statistics launch after it may start while it ends).
+__global__ void k_zero_counters(unsigned* done, int32_t* dev_error, int32_t* len_hist, int nh) {
+    grid_dep_wait();
+    grid_dep_trigger();
+    const int t = threadIdx.x;
+    if (t < 4) done[t] = 0u;
+    if (t == 0 && dev_error) *dev_error = 0;
+    if (len_hist)
+        for (int i = t; i < nh; i += blockDim.x) len_hist[i] = 0;
+}
+
 // Stage 1: statistics of every target and draft row into the workspace,
 // then the finishing launch (decisions and offsets).  bf16 rows under top-p
 // take the one-read kernel (rows_topp.cu) first; the finishing launch then
@@ -80,10 +94,9 @@ static spec_status launch_stats(LinearArgs& a, cudaStream_t st) {
         const spec_status r = launch_rows_topp_onepass(a, st);
         if (r != SPEC_OK) return r;
     } else {
-        k1<<<grid, kNT, dyn, st>>>(a, 0);
-        if (cudaGetLastError() != cudaSuccess) return SPEC_ERR_CUDA;
+        if (launch_dependent(k1, dim3(grid), dim3(kNT), dyn, st, a, 0) != cudaSuccess) return SPEC_ERR_CUDA;
     }
-    k1<<<grid, kNT, dyn, st>>>(a, 1);
+    if (launch_dependent(k1, dim3(grid), dim3(kNT), dyn, st, a, 1) != cudaSuccess) return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
@@ -159,10 +172,8 @@ extern "C" spec_status spec_linear_stats_decide(const void* target_logits, const
                                    params, workspace, workspace_bytes, a, mode);
     if (r != SPEC_OK) return r;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
-    if (len_hist && cudaMemsetAsync(len_hist, 0, sizeof(int32_t) * (size_t)(k + 1), st) != cudaSuccess)
+    if (launch_dependent(k_zero_counters, dim3(1), dim3(64), 0, st, a.done, dev_error, len_hist, k + 1) != cudaSuccess)
         return SPEC_ERR_CUDA;
-    if (cudaMemsetAsync(a.done, 0, 4 * sizeof(unsigned), st) != cudaSuccess) return SPEC_ERR_CUDA;
     a.acc_len = accepted_len;
     a.accept_prob = accept_prob;
     a.token_probs = token_probs;

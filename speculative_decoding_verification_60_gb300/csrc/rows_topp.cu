@@ -127,6 +127,8 @@ template <bool SAMPLE>
 __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_topp_onepass(LinearArgs a) {
     extern __shared__ __align__(128) uint8_t onepass_raw[];
     OnePassSmem& sm = *reinterpret_cast<OnePassSmem*>(onepass_raw);
+    grid_dep_wait();     // launched to overlap the launch before: wait for it before reading anything
+    grid_dep_trigger();  // the finishing launch may be scheduled; it waits for this grid
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int R = a.B * (2 * a.k + 1);
     const int V = a.V;
@@ -387,7 +389,8 @@ spec_status launch_rows_topp_onepass(LinearArgs& a, cudaStream_t st) {
     const size_t smem = sizeof(OnePassSmem);
     int grid = 0;
     if (!launch_grid(k_rows_topp_onepass<false>, smem, R, &grid, kOnePassThreads)) return SPEC_ERR_CUDA;
-    k_rows_topp_onepass<false><<<grid, kOnePassThreads, smem, st>>>(a);
+    if (launch_dependent(k_rows_topp_onepass<false>, dim3(grid), dim3(kOnePassThreads), smem, st, a) != cudaSuccess)
+        return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 

@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kNT, 2) k_sample_rows(SampleArgs a) {
     __shared__ SampleScratch ss;
     __shared__ DrawScratch ds;
     uint8_t* topsmem = reinterpret_cast<uint8_t*>(dyn_smem);
+    grid_dep_wait();  // after the one-read pass: its marks are in out
     for (int r = blockIdx.x; r < a.R; r += gridDim.x) {
         if (a.redo_only && a.out[r] != kSampleRedo) continue;  // the same for the whole CTA
         const T* row = static_cast<const T*>(a.logits) + (size_t)r * a.V;
@@ -66,7 +67,7 @@ static spec_status launch_sample(SampleArgs& a, cudaStream_t st) {
     auto* kern = k_sample_rows<T, MODE>;
     int grid = 0;
     if (!launch_grid(kern, dyn, a.R, &grid, kNT)) return SPEC_ERR_CUDA;
-    kern<<<grid, kNT, dyn, st>>>(a);
+    if (launch_dependent(kern, dim3(grid), dim3(kNT), dyn, st, a) != cudaSuccess) return SPEC_ERR_CUDA;
     return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
 
