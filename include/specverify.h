@@ -285,6 +285,31 @@ spec_status spec_verify_tree(const void* target_logits, const void* draft_logits
                              spec_stream_t stream);
 
 /*
+ * Tree verification with a tree of its own for every request (section
+ * "EAGLE": the tree explored is fixed (EAGLE) or dynamically shaped
+ * (EAGLE-2, in the page's citation); each request's tree is then its own).
+ * The walk at every node is spec_verify_tree's; only the shape differs:
+ *
+ *  parent  [B, N] int32   row b is request b's parent array over its nodes
+ *                         (parent[b, 0] = -1, 0 <= parent[b, i] < i).
+ *  n_nodes [B] int32      request b has nodes 0 .. n_nodes[b]-1; its rows,
+ *                         tokens and parent entries past them are not read.
+ *  target_logits, draft_logits [B, N, V] and node_tokens [B, N] as for
+ *  spec_verify_tree, N the largest tree; max_depth bounds every request's
+ *  depth (outputs have W = max_depth + 1 columns).
+ *  A request with n_nodes outside 1 .. N, or an invalid parent row, is
+ *  invalid (SPEC_DEVERR_PARENT) with the defined fallback.  n_nodes NULL
+ *  returns SPEC_ERR_INVALID_ARG; other host checks and limits as above.
+ */
+spec_status spec_verify_tree_dynamic(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                     const int32_t* node_tokens, const int32_t* parent, const int32_t* n_nodes,
+                                     int B, int N, int V, int max_depth, const int64_t* request_ids,
+                                     const int64_t* positions, const spec_sampling_params* params,
+                                     int32_t* accepted_len, int32_t* path_nodes, int32_t* out_tokens,
+                                     int32_t* dev_error, void* workspace, size_t workspace_bytes,
+                                     spec_stream_t stream);
+
+/*
  * Compaction for the next draft step (section "MTP": token t_{i+1} is drawn
  * from logits computed from hidden state H_i, so token buffers sit one step
  * left of the hidden states; section "MTP schedule for a single token": a

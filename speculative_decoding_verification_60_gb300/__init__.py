@@ -26,5 +26,6 @@ from ._binding import (  # noqa: F401
     verify_linear,
     verify_linear_compact,
     verify_tree,
+    verify_tree_dynamic,
     workspace_size,
 )

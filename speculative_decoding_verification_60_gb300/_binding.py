@@ -24,7 +24,8 @@ DEVERR_TOKEN, DEVERR_NONFINITE, DEVERR_PARENT, DEVERR_LENGTH = 1, 2, 4, 8
 
 # Every symbol declared in include/specverify.h.
 EXPORTS = ("spec_workspace_size", "spec_verify_linear", "spec_verify_linear_compact", "spec_linear_stats_decide",
-           "spec_linear_draw", "spec_verify_linear_noalloc", "spec_verify_tree", "spec_compact_accepted",
+           "spec_linear_draw", "spec_verify_linear_noalloc", "spec_verify_tree", "spec_verify_tree_dynamic",
+           "spec_compact_accepted",
            "spec_sample_rows", "spec_status_string")
 
 
@@ -72,6 +73,9 @@ def load() -> ctypes.CDLL:
     lib.spec_verify_tree.argtypes = [P, P, I, P, P, I, I, I, I, P, P, ctypes.POINTER(SamplingParams),
                                      P, P, P, P, P, Z, P]
     lib.spec_verify_tree.restype = I
+    lib.spec_verify_tree_dynamic.argtypes = [P, P, I, P, P, P, I, I, I, I, P, P, ctypes.POINTER(SamplingParams),
+                                             P, P, P, P, P, Z, P]
+    lib.spec_verify_tree_dynamic.restype = I
     lib.spec_compact_accepted.argtypes = [P, I, I, I, P, P, P, I, P, P, P, P, P]
     lib.spec_compact_accepted.restype = I
     lib.spec_sample_rows.argtypes = [P, I, I, I, P, P, ctypes.POINTER(SamplingParams), P, P, P]
@@ -238,6 +242,43 @@ def verify_tree(target, draft, node_tokens, parent, max_depth: int, temperature:
                               _ptr(out["dev_error"]), _ptr(ws), ws.numel(), _stream(stream))
     if st != SPEC_OK:
         raise SpecError("spec_verify_tree", st)
+    return out
+
+
+def verify_tree_dynamic(target, draft, node_tokens, parent, n_nodes, max_depth: int, temperature: float,
+                        top_p: float = 1.0, seed: int = 0, child_mode: int = CHILD_WOR, request_ids=None,
+                        positions=None, stream=None) -> dict:
+    """``spec_verify_tree_dynamic``: as verify_tree with a tree per request,
+    parent [B, N] int32 and n_nodes [B] int32 (device)."""
+    lib = load()
+    B, N, V = target.shape
+    dt = _dtype_code(target)
+    _check(target, "target")
+    _check(draft, "draft", target.dtype, (B, N, V))
+    _check(node_tokens, "node_tokens", torch.int32, (B, N))
+    _check(parent, "parent", torch.int32, (B, N))
+    _check(n_nodes, "n_nodes", torch.int32, (B,))
+    _check(request_ids, "request_ids", torch.int64, (B,))
+    _check(positions, "positions", torch.int64, (B,))
+    if n_nodes is None:
+        raise ValueError("n_nodes is required")
+    dev = target.device
+    W = int(max_depth) + 1
+    out = dict(
+        accepted_len=torch.empty(B, dtype=torch.int32, device=dev),
+        path_nodes=torch.empty(B, W, dtype=torch.int32, device=dev),
+        out_tokens=torch.empty(B, W, dtype=torch.int32, device=dev),
+        dev_error=torch.empty(1, dtype=torch.int32, device=dev),
+    )
+    need = workspace_size(SPEC_OP_TREE, B, N, V, dt)
+    ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    sp = SamplingParams(float(temperature), float(top_p), int(seed) & (2**64 - 1), int(child_mode))
+    st = lib.spec_verify_tree_dynamic(_ptr(target), _ptr(draft), dt, _ptr(node_tokens), _ptr(parent), _ptr(n_nodes),
+                                      B, N, V, int(max_depth), _ptr(request_ids), _ptr(positions), ctypes.byref(sp),
+                                      _ptr(out["accepted_len"]), _ptr(out["path_nodes"]), _ptr(out["out_tokens"]),
+                                      _ptr(out["dev_error"]), _ptr(ws), ws.numel(), _stream(stream))
+    if st != SPEC_OK:
+        raise SpecError("spec_verify_tree_dynamic", st)
     return out
 
 

@@ -4,7 +4,10 @@
 // One CTA walks one request's tree: at each node it takes the statistics of
 // the node's target (and draft) row, tests the children in index order with
 // the residual updates of recursive rejection sampling, and descends into
-// the first accepted child.
+// the first accepted child.  The tree is the same for every request (a
+// fixed tree, EAGLE) or each request's own (a dynamically shaped tree,
+// EAGLE-2 in the page's citation): parent [B, N] and a node count per
+// request, the walk itself unchanged.
 #include "../../include/specverify.h"
 #include "launch.cuh"
 #include "sample.cuh"
@@ -18,8 +21,10 @@ struct TreeArgs {
     const void* tgt;
     const void* drf;
     const int32_t* tok;
-    const int32_t* parent;
-    int B, N, V, W;  // W = max_depth + 1
+    const int32_t* parent;    // [N], or [B, N] with parent_stride = N
+    int parent_stride;        // 0: one tree for every request
+    const int32_t* n_nodes;   // [B] nodes of each request's tree, or NULL: N
+    int B, N, V, W;  // N: nodes (rows) per request in the inputs; W = max_depth + 1
     const int64_t* req;
     const int64_t* pos;
     float top_p, c;
@@ -71,18 +76,28 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
     const T* drf = a.drf ? static_cast<const T*>(a.drf) + (size_t)b * N * V : nullptr;
     const int32_t* tok = a.tok + (size_t)b * N;
     const bool use_q = (MODE > 0) && a.mode != SPEC_CHILD_DETERMINISTIC;
+    const int32_t* par = a.parent + (size_t)b * a.parent_stride;
+    int Nt = N;  // nodes of this request's tree
+    bool bad_count = false;
+    if (a.n_nodes) {
+        Nt = a.n_nodes[b];
+        if (Nt < 1 || Nt > N) {
+            bad_count = true;
+            Nt = 1;
+        }
+    }
 
     // Validate the parent array (depth <= max_depth) and the node tokens.
     if (tid == 0) {
-        int inval = 0;
-        if (a.parent[0] != -1) inval |= kDevErrParent;
+        int inval = bad_count ? kDevErrParent : 0;
+        if (par[0] != -1) inval |= kDevErrParent;
         sh_inval = inval;
     }
     __syncthreads();
     {
         int inval = 0;
-        for (int i = 1 + tid; i < N; i += kNT) {
-            const int p = a.parent[i];
+        for (int i = 1 + tid; i < Nt; i += kNT) {
+            const int p = par[i];
             if (p < 0 || p >= i) inval |= kDevErrParent;
             if (tok[i] < 0 || tok[i] >= V) inval |= kDevErrToken;
         }
@@ -93,8 +108,8 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
         // depth[i] = depth[parent[i]] + 1 (parent[i] < i was checked above)
         int dmax = 0;
         depth[0] = 0;
-        for (int i = 1; i < N; ++i) {
-            depth[i] = depth[a.parent[i]] + 1;
+        for (int i = 1; i < Nt; ++i) {
+            depth[i] = depth[par[i]] + 1;
             if (depth[i] > dmax) dmax = depth[i];
         }
         if (dmax > W - 1) sh_inval |= kDevErrParent;
@@ -111,9 +126,9 @@ __global__ void __launch_bounds__(kNT, 1) k_tree(TreeArgs a) {
         // children of n, in index order
         {
             int found = 0;
-            for (int c0 = n + 1; c0 < N; c0 += kNT) {  // children have larger indices than their parent
+            for (int c0 = n + 1; c0 < Nt; c0 += kNT) {  // children have larger indices than their parent
                 const int i = c0 + tid;
-                const bool is_child = (i < N && a.parent[i] == n);
+                const bool is_child = (i < Nt && par[i] == n);
                 int tot;
                 const int at = found + block_exclusive_scan_i(is_child ? 1 : 0, s, &tot);
                 if (is_child && at < kMaxChildren) ch[at] = i;
@@ -269,13 +284,11 @@ static spec_status launch_tree(TreeArgs& a, cudaStream_t st) {
 
 using namespace sv;
 
-extern "C" spec_status spec_verify_tree(const void* target_logits, const void* draft_logits, spec_dtype dtype,
-                                        const int32_t* node_tokens, const int32_t* parent, int B, int N, int V,
-                                        int max_depth, const int64_t* request_ids, const int64_t* positions,
-                                        const spec_sampling_params* params, int32_t* accepted_len,
-                                        int32_t* path_nodes, int32_t* out_tokens, int32_t* dev_error,
-                                        void* workspace, size_t workspace_bytes, spec_stream_t stream) {
-    DeviceGuard device_guard;  // the caller's current device is put back on return
+static spec_status tree_entry(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                              const int32_t* node_tokens, const int32_t* parent, int parent_stride,
+                              const int32_t* n_nodes, int B, int N, int V, int max_depth, const int64_t* request_ids,
+                              const int64_t* positions, const spec_sampling_params* params, int32_t* accepted_len,
+                              int32_t* path_nodes, int32_t* out_tokens, int32_t* dev_error, spec_stream_t stream) {
     if (!params || !target_logits || !node_tokens || !parent || !accepted_len || !path_nodes || !out_tokens)
         return SPEC_ERR_INVALID_ARG;
     if (dtype != SPEC_BF16 && dtype != SPEC_F32) return SPEC_ERR_INVALID_ARG;
@@ -288,8 +301,6 @@ extern "C" spec_status spec_verify_tree(const void* target_logits, const void* d
     const bool greedy = (T == 0.0f);
     if (!greedy && cm != SPEC_CHILD_DETERMINISTIC && !draft_logits) return SPEC_ERR_INVALID_ARG;
     if ((int64_t)V > kMaxVocab) return SPEC_ERR_UNSUPPORTED;
-    (void)workspace;
-    (void)workspace_bytes;
     if (!select_device_of(target_logits)) return SPEC_ERR_INVALID_ARG;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (dev_error && cudaMemsetAsync(dev_error, 0, sizeof(int32_t), st) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -298,6 +309,8 @@ extern "C" spec_status spec_verify_tree(const void* target_logits, const void* d
     a.drf = draft_logits;
     a.tok = node_tokens;
     a.parent = parent;
+    a.parent_stride = parent_stride;
+    a.n_nodes = n_nodes;
     a.B = B; a.N = N; a.V = V; a.W = max_depth + 1;
     a.req = request_ids;
     a.pos = positions;
@@ -318,4 +331,32 @@ extern "C" spec_status spec_verify_tree(const void* target_logits, const void* d
     if (mode == 0) return launch_tree<float, 0>(a, st);
     if (mode == 1) return launch_tree<float, 1>(a, st);
     return launch_tree<float, 2>(a, st);
+}
+
+extern "C" spec_status spec_verify_tree(const void* target_logits, const void* draft_logits, spec_dtype dtype,
+                                        const int32_t* node_tokens, const int32_t* parent, int B, int N, int V,
+                                        int max_depth, const int64_t* request_ids, const int64_t* positions,
+                                        const spec_sampling_params* params, int32_t* accepted_len,
+                                        int32_t* path_nodes, int32_t* out_tokens, int32_t* dev_error,
+                                        void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
+    (void)workspace;
+    (void)workspace_bytes;
+    return tree_entry(target_logits, draft_logits, dtype, node_tokens, parent, 0, nullptr, B, N, V, max_depth,
+                      request_ids, positions, params, accepted_len, path_nodes, out_tokens, dev_error, stream);
+}
+
+extern "C" spec_status spec_verify_tree_dynamic(const void* target_logits, const void* draft_logits,
+                                                spec_dtype dtype, const int32_t* node_tokens, const int32_t* parent,
+                                                const int32_t* n_nodes, int B, int N, int V, int max_depth,
+                                                const int64_t* request_ids, const int64_t* positions,
+                                                const spec_sampling_params* params, int32_t* accepted_len,
+                                                int32_t* path_nodes, int32_t* out_tokens, int32_t* dev_error,
+                                                void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    DeviceGuard device_guard;  // the caller's current device is put back on return
+    (void)workspace;
+    (void)workspace_bytes;
+    if (!n_nodes) return SPEC_ERR_INVALID_ARG;
+    return tree_entry(target_logits, draft_logits, dtype, node_tokens, parent, N, n_nodes, B, N, V, max_depth,
+                      request_ids, positions, params, accepted_len, path_nodes, out_tokens, dev_error, stream);
 }

@@ -79,6 +79,13 @@ def test_host_argument_checks_return_status(lib):
                                   None, None, None, None, dummy, 8, None) == 3
     assert lib.spec_verify_tree(dummy, dummy, 0, dummy, dummy, 1, 3, 8, 3, None, None, ctypes.byref(sp),
                                 dummy, dummy, dummy, None, dummy, 256, None) == 1
+    # the per-request tree call: n_nodes required; the limits of the static call
+    assert lib.spec_verify_tree_dynamic(dummy, dummy, 0, dummy, dummy, None, 1, 3, 8, 2, None, None,
+                                        ctypes.byref(sp), dummy, dummy, dummy, None, dummy, 256, None) == 1
+    assert lib.spec_verify_tree_dynamic(dummy, dummy, 0, dummy, dummy, dummy, 1, 3, 8, 3, None, None,
+                                        ctypes.byref(sp), dummy, dummy, dummy, None, dummy, 256, None) == 1
+    assert lib.spec_verify_tree_dynamic(dummy, dummy, 0, dummy, dummy, dummy, 1, 2000, 8, 2, None, None,
+                                        ctypes.byref(sp), dummy, dummy, dummy, None, dummy, 256, None) == 2
     assert lib.spec_compact_accepted(None, 1, 1, 8, dummy, None, dummy, 1, dummy, dummy, dummy, None, None) == 1
     # the compacting call needs its hidden buffers; the split calls check like the one-call form
     assert lib.spec_verify_linear_compact(dummy, dummy, 0, dummy, 1, 1, 8, None, None, ctypes.byref(sp), None, 16,
