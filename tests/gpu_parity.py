@@ -66,12 +66,13 @@ def row_topp_margin(tgt, drf, b, i, T, top_p) -> float:
     return m
 
 
-def compare_linear(got, ref, rows, greedy: bool, label: str = "", margin_of=None) -> int:
+def compare_linear(got, ref, rows, greedy: bool, label: str = "", margin_of=None, log=None) -> int:
     """Compare the GPU result for the batch rows `rows` with the oracle run
     on exactly those rows (ref indexed 0..len(rows)-1).  Returns the number
     of margin-excused mismatches.  margin_of(b, i), when given, is the
     top-p margin of drafted position i's rows (a boundary one token apart
-    shifts every probability of the row)."""
+    shifts every probability of the row).  log, when given, receives one
+    (request, kind, margin) entry per excused mismatch."""
     excused = 0
     for j, b in enumerate(rows):
         ga, ra = int(got["accepted_len"][b]), int(ref["accepted_len"][j])
@@ -85,6 +86,8 @@ def compare_linear(got, ref, rows, greedy: bool, label: str = "", margin_of=None
                     f"{label} request {b}: gpu a={ga} {gt.tolist()} oracle a={ra} {rt.tolist()} "
                     f"margin {ref['margin'][j]:.3g}")
                 excused += 1
+                if log is not None:
+                    log.append((b, "decision", float(ref["margin"][j])))
             tp = got["token_probs"][b].astype(np.float64)
             err = np.max(np.abs(tp - ref["tok_p"][j])) if tp.size else 0.0
             if err >= PROB_TOL:
@@ -94,6 +97,8 @@ def compare_linear(got, ref, rows, greedy: bool, label: str = "", margin_of=None
                 for i in bad_pos:
                     mg = margin_of(b, int(i)) if margin_of is not None else ref["margin"][j]
                     assert mg < MARGIN, f"{label} request {b} pos {i}: token probability error {err:.3g}, margin {mg:.3g}"
+                    if log is not None:
+                        log.append((b, "token probability", float(mg)))
                 excused += int(same)
             # accept_prob = min(1, p/q): consistent with the GPU's own p and q,
             # and close to the oracle's in relative terms (p/q amplifies q's error)

@@ -114,7 +114,7 @@ def test_bench_size_sampled_rows_and_slot_independence():
     x = synth.zipf_logits(R, V, seed=36)
     rng = np.random.default_rng(2)
     req, pos = rng.integers(0, 1 << 40, R), rng.integers(0, 1 << 20, R)
-    rows = sorted(rng.choice(R, 12, replace=False).tolist())
+    rows = sorted(rng.choice(R, 64, replace=False).tolist())
     got, err, excused = _check(x, 0.7, 0.9, 55, req, pos, rows=rows)
     assert err == 0 and excused <= 1
     # a row's token depends on (row, seed, request, position), not on its slot
