@@ -281,9 +281,12 @@ __global__ void __launch_bounds__(kDThreads, 2) k_draw_stream(LinearArgs a) {
                     cumP += cw & 0xffff;
                     cumQ += cw >> 16;
                 }
+                // the region holding the nP-th tau-valued token (the last one
+                // kept) locates it, also when it is the region's last: the
+                // re-read of the crossing region takes its thresholds from it
                 if (cntP) {
                     if (bp >= nP) tp = P.above2;
-                    else if (bp + rcp > nP) {  // the cut lies in this region
+                    else if (bp + rcp >= nP) {  // the cut lies in this region
                         P.cut = locate_cut(vp, P.tau, u0, bp, nP - 1);
                         if (lane == 0) sm.cut[0] = P.cut;
                         exact = true;
@@ -291,7 +294,7 @@ __global__ void __launch_bounds__(kDThreads, 2) k_draw_stream(LinearArgs a) {
                 }
                 if (cntQ) {
                     if (bq >= nQ) tq = Q.above2;
-                    else if (bq + rcq > nQ) {
+                    else if (bq + rcq >= nQ) {
                         Q.cut = locate_cut(vq, Q.tau, u0, bq, nQ - 1);
                         if (lane == 0) sm.cut[1] = Q.cut;
                         exact = true;

@@ -73,3 +73,69 @@ def test_bench_workload_32_requests():
     _hist_check(got, ref, rows, k, excused)
     assert got["len_hist"].sum() == B
     assert np.array_equal(got["len_hist"], np.bincount(got["accepted_len"], minlength=k + 1))
+
+
+@pytest.mark.parametrize("T,top_p", [(0.8, 0.9), (1.0, 1.0)])
+def test_one_request_under_a_thousand_request_ids(T, top_p):
+    """The rows of one request (k = 1, V = 20000) replicated under 1024
+    request ids: the draws then probe the whole CDF of the request's
+    residual and bonus distributions.  Every token must be the oracle's."""
+    R, k, V, seed = 1024, 1, 20000, 4242
+    tgt1, drf1 = synth.linear_logits(1, k, V, "bf16", 2718)
+    tgt = tgt1.expand(R, k + 1, V).contiguous()
+    drf = drf1.expand(R, k, V).contiguous()
+    # half the requests draft a token inside both nuclei, half a uniform token
+    d = np.zeros((R, k), dtype=np.int32)
+    d[: R // 2] = draft_tokens_from_oracle(drf1, T, top_p, seed=3)[0]
+    d[R // 2:] = synth.uniform_tokens((R - R // 2, k), V, 11).numpy()
+    req = np.arange(R, dtype=np.int64) * 104729 + 17
+    pos = np.full(R, 9, dtype=np.int64)
+    got = run_gpu_linear(tgt, drf, d, T, top_p, seed, req, pos)
+    rows = list(range(R))
+    ref = oracle_linear(tgt, drf, d, T, top_p, seed, req, pos, rows)
+    log = []
+    excused = compare_linear(got, ref, rows, greedy=False, label=f"1024 ids T={T} p={top_p}",
+                             margin_of=lambda b, i: row_topp_margin(tgt1, drf1, 0, i, T, top_p), log=log)
+    # one row pair: its top-p margin is the same for every request
+    assert excused <= 4, log
+    _hist_check(got, ref, rows, k, excused)
+    # the draws spread over the distributions
+    t_star = got["out_tokens"][np.arange(R), got["accepted_len"]]
+    assert len(np.unique(t_star)) > R // 20
+
+
+def test_cut_at_the_end_of_a_region():
+    """Top-p keeps the first n_keep tokens valued exactly at the boundary
+    value tau, in index order.  Here the last kept one is the last
+    tau-valued token of the first 1024 elements, so the tau-valued tokens
+    after it are dropped everywhere after that point; 64 bonus draws over the
+    row (target row 0 equals draft row 0, so every draft is accepted) must
+    match the oracle and never return a dropped token."""
+    V, B, k, T, seed = 8192, 64, 1, 1.0, 99
+    x = np.full(V, -20.0, dtype=np.float32)
+    big = [100, 2100, 3100, 4100, 5100, 6100, 7100, 8100]
+    x[big] = 4.0
+    taus = [10, 500, 1000, 1100, 1500, 2000, 3500, 3600, 3700]
+    x[taus] = 1.0
+    w = np.exp(x.astype(np.float64) - 4.0)
+    top_p = float((w[big].sum() + 2.5 * w[taus[0]]) / w.sum())  # keeps exactly the first three tau-valued
+    import oracle
+
+    p = oracle.row_probs(x, T, top_p)[0]
+    assert [int(p[t] > 0) for t in taus] == [1, 1, 1, 0, 0, 0, 0, 0, 0]
+    g = torch.Generator().manual_seed(5)
+    row0 = torch.randn(V, generator=g)
+    tgt = torch.stack([row0, torch.from_numpy(x)]).unsqueeze(0).expand(B, 2, V).contiguous().to(torch.bfloat16)
+    drf = row0.unsqueeze(0).unsqueeze(0).expand(B, 1, V).contiguous().to(torch.bfloat16)
+    d = np.full((B, k), int(torch.argmax(row0)), dtype=np.int32)
+    req = np.arange(B, dtype=np.int64) * 31 + 7
+    pos = np.zeros(B, dtype=np.int64)
+    got = run_gpu_linear(tgt, drf, d, T, top_p, seed, req, pos)
+    assert (got["accepted_len"] == 1).all()
+    dropped = set(taus[3:])
+    assert not any(int(t) in dropped for t in got["out_tokens"][:, 1])
+    rows = list(range(B))
+    ref = oracle_linear(tgt, drf, d, T, top_p, seed, req, pos, rows)
+    assert compare_linear(got, ref, rows, greedy=False, label="cut at a region end") == 0
+    # the draws reach past the cut
+    assert (got["out_tokens"][:, 1] > 1000).sum() > B // 4
