@@ -464,11 +464,46 @@ def time_tree(device, K: int, W: int, peak: float):
     path_bytes = visited * 2 * V * 2
     all_bytes = B * N * 2 * V * 2
     gbps = path_bytes / (ms / 1e3) / 1e9
-    return {"workload": TREE_WORKLOAD, "ms_per_step": round(ms, 4), "requests": B, "child_mode": "wor",
-            "children": "distinct tokens drawn without replacement from the parent's draft row",
-            "visited_nodes": visited, "visited_nodes_per_s": round(visited / (ms / 1e3), 1),
-            "mean_accepted_depth": float(np.mean(acc)), "path_bytes": path_bytes, "all_nodes_bytes": all_bytes,
-            "path_gbps": round(gbps, 1), "frac": round(gbps / peak, 4)}
+    res = {"workload": TREE_WORKLOAD, "ms_per_step": round(ms, 4), "requests": B, "child_mode": "wor",
+           "children": "distinct tokens drawn without replacement from the parent's draft row",
+           "visited_nodes": visited, "visited_nodes_per_s": round(visited / (ms / 1e3), 1),
+           "mean_accepted_depth": float(np.mean(acc)), "path_bytes": path_bytes, "all_nodes_bytes": all_bytes,
+           "path_gbps": round(gbps, 1), "frac": round(gbps / peak, 4)}
+
+    # a tree per request (spec_verify_tree_dynamic): request b keeps the
+    # n_b best nodes of the same top-4, depth-5 tree, n_b from 20 to 60
+    counts = np.array([20 + (b * 7) % 41 for b in range(B)], dtype=np.int32)
+    parents = np.zeros((B, N), dtype=np.int32)
+    tok_d = torch.zeros(B, N, dtype=torch.int32, device=device)
+    for b in range(B):
+        pb = synth.pruned_tree(w["K"], w["depth"], int(counts[b]))
+        parents[b, :len(pb)] = pb
+        for n in range(len(pb)):
+            kids = [i for i in range(1, len(pb)) if pb[i] == n]
+            if kids:
+                p = torch.softmax(drf[b, n].float() / w["T"], -1)
+                tok_d[b, kids] = torch.multinomial(p, len(kids), replacement=False, generator=g).to(torch.int32)
+    parents_d = torch.as_tensor(parents, device=device)
+    counts_d = torch.as_tensor(counts, device=device)
+    for _ in range(W):
+        out = svp.verify_tree_dynamic(tgt, drf, tok_d, parents_d, counts_d, w["depth"], w["T"], w["top_p"],
+                                      w["seed"], svp.CHILD_WOR)
+    torch.cuda.synchronize()
+    e0.record()
+    for _ in range(K):
+        out = svp.verify_tree_dynamic(tgt, drf, tok_d, parents_d, counts_d, w["depth"], w["T"], w["top_p"],
+                                      w["seed"], svp.CHILD_WOR)
+    e1.record()
+    torch.cuda.synchronize()
+    ms_d = e0.elapsed_time(e1) / K
+    acc_d = out["accepted_len"].cpu().numpy()
+    visited_d = int(np.sum(acc_d + 1))
+    gbps_d = visited_d * 2 * V * 2 / (ms_d / 1e3) / 1e9
+    res["dynamic"] = {"nodes_per_request": f"{int(counts.min())}..{int(counts.max())} (mean {float(counts.mean()):.1f})",
+                      "ms_per_step": round(ms_d, 4), "visited_nodes": visited_d,
+                      "mean_accepted_depth": float(np.mean(acc_d)), "path_gbps": round(gbps_d, 1),
+                      "frac": round(gbps_d / peak, 4), "dev_error": int(out["dev_error"].cpu()[0])}
+    return res
 
 
 # The other workloads the method's pages describe, timed beside the headline

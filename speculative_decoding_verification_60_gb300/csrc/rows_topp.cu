@@ -318,7 +318,12 @@ __global__ void __launch_bounds__(kOnePassThreads, kOnePassCtasPerSm) k_rows_top
         // or weights too large for fp32 relative to m^); a finite sum also
         // bounds every key's mass below
         bool redo = abort_row || !est || sm.hist[kWinKeys - 1] != 0u || !(zr.hi > 0.0f && zr.hi < INFINITY);
-        if (!redo) {
+        if (redo) {
+            // every thread has read the sentinel and xtok before the next row
+            // clears the histogram and writes xtok (the walk's barriers do
+            // this on the other branch), so all take the same branch
+            row_sync();
+        } else {
             const float mc = scaled_max(mh, c);
             const ff pZ = ff_mul_f(zr, top_p);
             // positions 1 .. kWinKeys-2 walked down from the top by the block
