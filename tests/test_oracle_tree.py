@@ -94,3 +94,35 @@ def test_bad_parent_array_is_flagged():
     out = oracle.verify_tree(np.zeros((1, 3, 4)), np.zeros((1, 3, 4)), np.zeros((1, 3), np.int32),
                              np.array([-1, 2, 0], np.int32), 1.0, 1.0, seed=0)
     assert out["dev_error"] & oracle.ERR_PARENT
+
+
+@pytest.mark.parametrize("mode", [oracle.CHILD_WOR, oracle.CHILD_IID, oracle.CHILD_DET])
+def test_a_request_depends_only_on_its_own_tree(mode):
+    """Per-request trees (§EAGLE: fixed or dynamically shaped trees) are read
+    as the fixed-tree walk applied to each request's own tree.  That reading
+    needs a request's result to depend only on its rows, tree, request id
+    and position: the batched oracle's result for a request equals the
+    oracle on that request alone, and a request keeps its result when the
+    other requests of the batch change."""
+    rng = np.random.default_rng(60 + mode)
+    B, V = 6, 9
+    for name, parent in TREES.items():
+        N = len(parent)
+        tgt = rng.normal(0, 1.2, (B, N, V))
+        drf = tgt + rng.normal(0, 0.6, (B, N, V))
+        tok = rng.integers(0, V, (B, N)).astype(np.int32)
+        req = np.arange(B, dtype=np.int64) * 5 + 2
+        pos = np.arange(B, dtype=np.int64) + 7
+        for T, tp in ((1.0, 1.0), (0.8, 0.9)):
+            batch = oracle.verify_tree(tgt, drf, tok, parent, T, tp, seed=23, mode=mode, req_ids=req, positions=pos)
+            other = tgt.copy()
+            other[1:] = rng.normal(0, 1.2, other[1:].shape)  # the rest of the batch changes
+            batch2 = oracle.verify_tree(other, drf, tok, parent, T, tp, seed=23, mode=mode, req_ids=req,
+                                        positions=pos)
+            for b in range(B):
+                one = oracle.verify_tree(tgt[b:b + 1], drf[b:b + 1], tok[b:b + 1], parent, T, tp, seed=23, mode=mode,
+                                         req_ids=req[b:b + 1], positions=pos[b:b + 1])
+                for key in ("accepted_len", "path_nodes", "out_tokens"):
+                    assert np.array_equal(batch[key][b], one[key][0]), (name, b, key)
+                    if b == 0:
+                        assert np.array_equal(batch2[key][0], one[key][0]), (name, key)
