@@ -41,6 +41,11 @@
  *  - Each call makes the device that holds its logits (or hidden states)
  *    current for its own launches and puts the caller's current device
  *    back before it returns.
+ *  - The linear calls and the draft-side sampler use dependent launches:
+ *    a launch may be scheduled while the kernel before it on the stream is
+ *    ending, and waits for that kernel to complete before it reads or
+ *    writes anything.  Stream order is kept; after any other stream
+ *    operation (a copy, an event) they are ordinary launches.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H
@@ -164,7 +169,7 @@ spec_status spec_verify_linear(const void* target_logits, const void* draft_logi
  * with no host synchronisation).  Results as spec_verify_linear followed by
  * spec_compact_accepted(hidden, B, k+1, H, accepted_len, NULL, out_tokens,
  * k+1, out_hidden, offsets, next_tokens, ...), without the compaction's own
- * launch: the last CTA of the row-statistics launch takes every request's
+ * launch: the launch after the row statistics takes every request's
  * decisions and the packed offsets, and each request's draw CTA copies its
  * a_b + 1 hidden rows and writes their next tokens.
  *
@@ -193,8 +198,8 @@ spec_status spec_verify_linear_compact(const void* target_logits, const void* dr
  * spec_verify_linear_compact), for callers that want to time them apart or
  * start the streaming pass as soon as the logits exist.
  * spec_linear_stats_decide reads every target row (and every draft row when
- * T > 0) once, writes per-row statistics into `workspace`, and in the last
- * CTA of that launch runs every request's accept tests: it writes
+ * T > 0) once, writes per-row statistics into `workspace`, and in a
+ * finishing launch runs every request's accept tests: it writes
  * accepted_len, accept_prob, token_probs, len_hist and dev_error (zeroing
  * len_hist and dev_error first) and keeps each request's decision and the
  * packed offsets in the workspace.  spec_linear_draw then draws every

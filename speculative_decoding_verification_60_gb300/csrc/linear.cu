@@ -1,9 +1,11 @@
 // Linear verification ("Accelerating Sonar through speculation",
 // §Speculative decoding and §Target-Draft): row statistics of every target
-// and draft row, and in the last CTA of that launch every request's accept
-// tests, accepted length and packed offsets (this file); then per request
-// the residual or bonus draw and, for the compacting call, the gather of the
-// accepted positions' hidden rows (decide.cu); the C entry points.
+// and draft row (this file's two-pass kernel, or the one-read kernel of
+// rows_topp.cu for bf16 rows under top-p), then a finishing launch that
+// takes every request's accept tests, accepted length and packed offsets
+// (this file); then per request the residual or bonus draw and, for the
+// compacting call, the gather of the accepted positions' hidden rows
+// (draw_stream.cu, decide.cu); the C entry points.
 #include <mutex>
 
 #include "../../include/specverify.h"
